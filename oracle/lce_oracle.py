@@ -1,0 +1,252 @@
+"""fp64 CPU oracle for the fused LM-head linear + cross-entropy (TEST INFRASTRUCTURE).
+
+This is the plain, slow, obviously correct definition of what the CUDA path
+computes. Only the tests, the smoke check and the benchmark's CPU-baseline leg
+may import it; the product path never does. It shares no code with the CUDA
+path (the two only share the seeded input generator, which does no loss
+arithmetic).
+
+What is computed (the definition, written out):
+  "XTuner on Ascend 910C: Qwen3.5-2B training optimisation", section 3.1.4
+  (Liger chunked cross-entropy, Fig. 12): the loss chain turns the LM-head
+  logits of an mbs x seq x vocab batch into a token-level cross-entropy and
+  back-propagates it to d_input and d_weight; the fused kernel never keeps the
+  full d_logits. The formula itself is the standard token-level
+  cross-entropy with ignore_index and a mean over valid tokens:
+
+    z      = H W^T                               [N, V]   (fp64, exact products)
+    lse_i  = m_i + log sum_v exp(z_iv - m_i),    m_i = max_v z_iv
+    loss_i = valid_i * (lse_i - z_{i, y_i})
+    L      = sum_i loss_i / n        (mean)   or   sum_i loss_i   (sum)
+    G_iv   = valid_i * g * (exp(z_iv - lse_i) - [v = y_i]) / n   (mean; no /n for sum)
+    dH     = G W                                 [N, d]
+    dW     = G^T H                               [V, d]
+
+with valid_i = [y_i != ignore_index] and n = sum_i valid_i (or a caller-given
+global count, the data-parallel denominator). Readings where the pages are
+silent: n = 0 gives L = 0 and G = 0; lse is computed for every row, ignored
+ones included; a label equal to ignore_index is ignored even inside [0, V);
+any other label outside [0, V) is an error.
+
+The row-block loop below is the token chunking the method itself prescribes
+("XTuner V1 introduction", memory optimisation section: the loss graph is
+computed in chunks); ``lce_chunked_online`` additionally splits the
+vocabulary into tiles with the streaming max/sum-exp update of
+"MindSpeed fusion optimisation: principles and practice", section 3.2
+(blockwise softmax without the full score matrix), and must agree with the
+unchunked result to rounding.
+
+Matrix products use numpy's fp64 matmul as a library step. Inputs are bf16
+bit patterns (uint16) decoded exactly to fp64.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+IGNORE_INDEX = -100
+MEAN, SUM = 0, 1
+
+
+class LabelRangeError(ValueError):
+    """A label is neither ignore_index nor inside [0, V)."""
+
+
+def decode_bf16(bits) -> np.ndarray:
+    """bf16 bit patterns -> fp64, exactly (bits << 16 is the fp32 pattern)."""
+    b = np.ascontiguousarray(np.asarray(bits, dtype=np.uint16))
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _prepare(y, V, ignore_index, reduction, n_valid_override, grad_loss):
+    y = np.asarray(y, dtype=np.int64)
+    valid = y != ignore_index
+    bad = valid & ((y < 0) | (y >= V))
+    if bad.any():
+        raise LabelRangeError(f"{int(bad.sum())} labels outside [0, {V}) and != {ignore_index}")
+    n = int(valid.sum()) if n_valid_override is None or n_valid_override < 0 else int(n_valid_override)
+    if reduction == MEAN:
+        scale = 0.0 if n == 0 else float(grad_loss) / n
+        lscale = 0.0 if n == 0 else 1.0 / n
+    elif reduction == SUM:
+        scale, lscale = float(grad_loss), 1.0
+    else:
+        raise ValueError("reduction must be MEAN (0) or SUM (1)")
+    return y, valid, n, scale, lscale
+
+
+def lce_f64(H, W, y, *, ignore_index=IGNORE_INDEX, reduction=MEAN,
+            n_valid_override=-1, grad_loss=1.0, row_block=256, grads=True):
+    """The definition on fp64 arrays H [N, d], W [V, d], labels y [N].
+
+    Returns dict(loss, lse, loss_i, zt, n_valid, dH, dW) (dH/dW only if grads).
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    N, d = H.shape
+    V = W.shape[0]
+    y, valid, n, scale, lscale = _prepare(y, V, ignore_index, reduction,
+                                          n_valid_override, grad_loss)
+    lse = np.empty(N)
+    loss_i = np.zeros(N)
+    zt = np.zeros(N)
+    dH = np.zeros((N, d)) if grads else None
+    dW = np.zeros((V, d)) if grads else None
+    for r0 in range(0, N, row_block):
+        r1 = min(N, r0 + row_block)
+        rows = np.arange(r0, r1)
+        z = H[r0:r1] @ W.T                                  # logits of this chunk
+        m = z.max(axis=1)
+        s = np.exp(z - m[:, None]).sum(axis=1)
+        lse[r0:r1] = m + np.log(s)
+        v = valid[r0:r1]
+        yy = np.where(v, y[r0:r1], 0)
+        zt[r0:r1] = np.where(v, z[rows - r0, yy], 0.0)
+        loss_i[r0:r1] = np.where(v, lse[r0:r1] - zt[r0:r1], 0.0)
+        if grads:
+            p = np.exp(z - lse[r0:r1, None])                # softmax
+            p[(rows - r0)[v], yy[v]] -= 1.0                 # minus one-hot
+            G = p * (v * scale)[:, None]
+            dH[r0:r1] = G @ W
+            dW += G.T @ H[r0:r1]
+    loss = math.fsum(loss_i.tolist()) * lscale
+    out = {"loss": loss, "lse": lse, "loss_i": loss_i, "zt": zt, "n_valid": n}
+    if grads:
+        out["dH"], out["dW"] = dH, dW
+    return out
+
+
+def lce_bf16(Hbits, Wbits, y, **kw):
+    """``lce_f64`` on bf16 bit-pattern inputs (the CUDA path's input format)."""
+    return lce_f64(decode_bf16(Hbits), decode_bf16(Wbits), y, **kw)
+
+
+def lce_chunked_online(H, W, y, *, chunk=64, vtile=32, ignore_index=IGNORE_INDEX,
+                       reduction=MEAN, n_valid_override=-1, grad_loss=1.0):
+    """Chunked tokens x tiled vocabulary with the streaming (m, s) update.
+
+    For each token chunk, the vocabulary is visited tile by tile and each row
+    keeps a running max m and a running sum s of exp(z - m):
+        m' = max(m, max_T z),  s' = s * exp(m - m') + sum_T exp(z - m').
+    The gradient is formed per (chunk, tile) once lse is known and summed into
+    dH (over tiles) and dW (over chunks). Must equal ``lce_f64`` to rounding.
+    """
+    H = np.asarray(H, dtype=np.float64)
+    W = np.asarray(W, dtype=np.float64)
+    N, d = H.shape
+    V = W.shape[0]
+    y, valid, n, scale, lscale = _prepare(y, V, ignore_index, reduction,
+                                          n_valid_override, grad_loss)
+    lse = np.empty(N)
+    loss_i = np.zeros(N)
+    dH = np.zeros((N, d))
+    dW = np.zeros((V, d))
+    for c0 in range(0, N, chunk):
+        c1 = min(N, c0 + chunk)
+        Hc = H[c0:c1]
+        m = np.full(c1 - c0, -np.inf)
+        s = np.zeros(c1 - c0)
+        zt = np.zeros(c1 - c0)
+        for t0 in range(0, V, vtile):
+            t1 = min(V, t0 + vtile)
+            z = Hc @ W[t0:t1].T
+            m_new = np.maximum(m, z.max(axis=1))
+            s = s * np.exp(m - m_new) + np.exp(z - m_new[:, None]).sum(axis=1)
+            m = m_new
+            for r in range(c1 - c0):
+                yi = y[c0 + r]
+                if valid[c0 + r] and t0 <= yi < t1:
+                    zt[r] = z[r, yi - t0]
+        lse_c = m + np.log(s)
+        lse[c0:c1] = lse_c
+        v = valid[c0:c1]
+        loss_i[c0:c1] = np.where(v, lse_c - zt, 0.0)
+        for t0 in range(0, V, vtile):
+            t1 = min(V, t0 + vtile)
+            z = Hc @ W[t0:t1].T
+            p = np.exp(z - lse_c[:, None])
+            for r in range(c1 - c0):
+                yi = y[c0 + r]
+                if v[r] and t0 <= yi < t1:
+                    p[r, yi - t0] -= 1.0
+            G = p * (v * scale)[:, None]
+            dH[c0:c1] += G @ W[t0:t1]
+            dW[t0:t1] += G.T @ Hc
+    loss = math.fsum(loss_i.tolist()) * lscale
+    return {"loss": loss, "lse": lse, "loss_i": loss_i, "n_valid": n, "dH": dH, "dW": dW}
+
+
+# ---------------------------------------------------------------------------
+# Sampled evaluation for full-size workloads: each function computes exactly
+# the same quantities as ``lce_f64`` for a subset of outputs.
+# ---------------------------------------------------------------------------
+
+def forward_rows_f64(H, W, y, rows=None, *, ignore_index=IGNORE_INDEX, row_block=128):
+    """lse_i, loss_i (unscaled) and z_{i,y_i} for the given rows (all by default).
+
+    ``W`` may be fp32 (exact for bf16 inputs); every product is done in fp64.
+    """
+    N = H.shape[0]
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    y = np.asarray(y, dtype=np.int64)
+    W64 = np.asarray(W, dtype=np.float64)
+    lse = np.empty(rows.size)
+    zt = np.zeros(rows.size)
+    for b0 in range(0, rows.size, row_block):
+        rb = rows[b0:b0 + row_block]
+        z = np.asarray(H[rb], dtype=np.float64) @ W64.T
+        m = z.max(axis=1)
+        lse[b0:b0 + rb.size] = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+        yy = y[rb]
+        v = yy != ignore_index
+        zt[b0:b0 + rb.size] = np.where(v, z[np.arange(rb.size), np.where(v, yy, 0)], 0.0)
+    valid = y[rows] != ignore_index
+    loss_i = np.where(valid, lse - zt, 0.0)
+    return {"rows": rows, "lse": lse, "zt": zt, "loss_i": loss_i}
+
+
+def grad_scale(y, *, ignore_index=IGNORE_INDEX, reduction=MEAN, n_valid_override=-1,
+               grad_loss=1.0):
+    """The factor g/n (mean) or g (sum) that multiplies softmax - one-hot."""
+    y = np.asarray(y)
+    n = int((y != ignore_index).sum()) if n_valid_override < 0 else int(n_valid_override)
+    if reduction == SUM:
+        return float(grad_loss), n
+    return (0.0 if n == 0 else float(grad_loss) / n), n
+
+
+def dH_rows_f64(H, W, y, rows, scale, *, ignore_index=IGNORE_INDEX):
+    """dH_i = sum_v G_iv W_v for the given rows (lse recomputed per row)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    y = np.asarray(y, dtype=np.int64)
+    W64 = np.asarray(W, dtype=np.float64)
+    out = np.zeros((rows.size, W64.shape[1]))
+    for j, i in enumerate(rows):
+        if y[i] == ignore_index:
+            continue
+        z = np.asarray(H[i], dtype=np.float64) @ W64.T
+        m = z.max()
+        lse = m + math.log(np.exp(z - m).sum())
+        p = np.exp(z - lse)
+        p[y[i]] -= 1.0
+        out[j] = (p * scale) @ W64
+    return out
+
+
+def dW_rows_f64(H, W, y, lse, vrows, scale, *, ignore_index=IGNORE_INDEX):
+    """dW_v = sum_i G_iv H_i for the given vocabulary rows.
+
+    ``lse`` must be the oracle's own per-row log-sum-exp for all N rows.
+    """
+    vrows = np.asarray(vrows, dtype=np.int64)
+    y = np.asarray(y, dtype=np.int64)
+    H64 = np.asarray(H, dtype=np.float64)
+    Wv = np.asarray(W[vrows], dtype=np.float64)
+    z = H64 @ Wv.T                                # [N, |S|]
+    p = np.exp(z - np.asarray(lse)[:, None])
+    valid = y != ignore_index
+    for j, v in enumerate(vrows):
+        p[valid & (y == v), j] -= 1.0
+    G = p * (valid * scale)[:, None]
+    return G.T @ H64
