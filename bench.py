@@ -1,0 +1,380 @@
+"""Benchmark of the fused chunked LM-head linear + cross-entropy (forward + backward).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--chunk C]
+
+One step = one lce_fwd_bwd call over the whole batch: logits GEMMs with the
+streaming log-sum-exp epilogue, gradient tiles, dH and dW GEMMs, loss
+reduction, on synthetic inputs of the Qwen3.5-2B-like LM-head workload
+(N = 8192 tokens, d = 2048, V = 151936; H ~ N(0,1) bf16, W ~ N(0, 0.02) bf16,
+uniform labels, 5% ignored at packed-document starts, seed 0).
+
+Prints ONE JSON line (rank 0). Metric: tokens/s of the fused fwd+bwd, with
+TFLOP/s counted as 6*N*V*d per step and its fraction of the dense bf16 peak.
+``value`` is device-resident throughput; ``e2e`` repeats it through the same
+public call with the step's inputs copied from pinned host memory and the
+loss read back every step. Inputs (W 0.62 GB, dW 1.24 GB, gradient tiles
+> 1 GB) are larger than the 129 MB L2, so no separate L2 flush is done.
+
+Multi-GPU (torchrun, one rank per GPU): data parallel over tokens, weak
+scaling. Each rank holds its own 8192-token shard; the global count of valid
+tokens is all-reduced once, every step runs lce_fwd_bwd with that global
+denominator and all-reduces dW (sum) and the loss (sum) over NCCL.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead
+(rank 0 only), each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from chunked_lm_head_linear_gb300 import inputs  # noqa: E402
+
+METRIC = "tokens/s fused linear-CE fwd+bwd (d=2048,V=151936); % of BF16 tensor peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            try:
+                sm.append(float(parts[2].split()[0]))
+                smax.append(float(parts[3].split()[0]))
+                power.append(float(parts[4].split()[0]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, parts[6:10]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch):
+    try:
+        u = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+        return u.replace("GPU-", "")
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (reported baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample_time(inp, rows: int):
+    """Time the fp64 oracle (fwd + bwd, full V and d) on the first ``rows`` tokens."""
+    import oracle
+    H = oracle.decode_bf16(inp["H"][:rows])
+    W = oracle.decode_bf16(inp["W"])
+    y = inp["y"][:rows]
+    t0 = time.perf_counter()
+    oracle.lce_f64(H, W, y)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(inp, target_s=12.0, max_rows=2048):
+    t16 = oracle_sample_time(inp, 16)
+    rows = int(min(max_rows, max(16, 16 * target_s / max(t16, 1e-3))))
+    rows = max(16, rows // 16 * 16)
+    t = oracle_sample_time(inp, rows)
+    return {"value": rows / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"first {rows} tokens of the workload at full d and V, numpy fp64 oracle "
+                      f"(forward + backward), {t:.1f} s; BLAS threads = all host cores"}
+
+
+def run_reference(args, w):
+    """--impl reference: the CPU oracle, each step a bounded sample of the workload."""
+    import oracle
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    inp = inputs.make_inputs(w)
+    Hd = oracle.decode_bf16(inp["H"])
+    Wd = oracle.decode_bf16(inp["W"])
+    y = inp["y"]
+    t16 = time.perf_counter()
+    oracle.lce_f64(Hd[:16], Wd, y[:16])
+    t16 = time.perf_counter() - t16
+    budget = 150.0 / max(1, args.steps + args.warmup)     # whole run within a few minutes
+    rows = int(max(16, min(w.N, 16 * budget / max(t16, 1e-3))) // 16 * 16)
+    for s in range(args.warmup):
+        oracle.lce_f64(Hd[:rows], Wd, y[:rows])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        r0 = (s * rows) % max(1, w.N - rows + 1)
+        oracle.lce_f64(Hd[r0:r0 + rows], Wd, y[r0:r0 + rows])
+    dt = time.perf_counter() - t0
+    value = rows * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(w, None, args),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{rows} tokens per step at full d and V (numpy fp64 oracle, fwd+bwd)"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w, chunk, args):
+    return {"workload": w.name, "N_tokens_per_gpu": w.N, "d": w.d, "V": w.V, "chunk_tokens": chunk,
+            "labels": w.labels, "ignore": w.ignore, "seed": w.seed,
+            "global_batch_tokens": w.N * args.gpus, "parallelism": f"dp{args.gpus}",
+            "l2": "inputs larger than L2 (W 0.62 GB, dW 1.24 GB, gradient tiles > 1 GB); no flush"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--chunk", type=int, default=4096)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from chunked_lm_head_linear_gb300 import lce
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    lce.load()
+    dev = torch.device("cuda", local)
+
+    # weak scaling: each rank draws its own shard (seed = rank)
+    inp = inputs.make_inputs(w, seed=w.seed + rank)
+    N, d, V = w.N, w.d, w.V
+    H_host = torch.from_numpy(inp["H"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_host = torch.from_numpy(inp["y"]).pin_memory()
+    W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    H = H_host.to(dev)
+    y = y_host.to(dev)
+    n_local = int((inp["y"] != inputs.IGNORE_INDEX).sum())
+    n_global = n_local
+    if world > 1:
+        t = torch.tensor([n_local], dtype=torch.int64, device=dev)
+        dist.all_reduce(t)
+        n_global = int(t.item())
+
+    chunk = min(args.chunk, N) if args.chunk > 0 else 0
+    opts = dict(chunk_tokens=chunk, n_valid_override=n_global if world > 1 else -1)
+    ws = torch.empty(lce.workspace_size(lce.LCE_OP_FWD_BWD, N, d, V, lce.make_opts(**opts)), dtype=torch.uint8,
+                     device=dev)
+    dW = torch.empty((V, d), dtype=torch.float32, device=dev)
+    lse = torch.empty(N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(Hx, yx):
+        loss, _, dH, _ = lce.lce_fwd_bwd(Hx, W, yx, dW=dW, lse=lse, workspace=ws, **opts)
+        if world > 1:
+            dist.all_reduce(dW)
+            dist.all_reduce(loss)
+        return loss, dH
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident throughput, kernels timed by events on their stream
+    for _ in range(args.warmup):
+        step(H, y)
+    barrier()
+    clocks = ClockSampler(gpu_uuid(torch))
+    clocks.start()
+    time.sleep(0.3)
+    lce.profile_begin()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(H, y)
+    ev1.record(stream)
+    barrier()
+    prof = lce.profile_end()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = N * world * args.steps / (ms * 1e-3)
+
+    # ---- end to end through the same public call, host buffers
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    for _ in range(2):
+        H.copy_(H_host, non_blocking=True)
+        y.copy_(y_host, non_blocking=True)
+        loss, _ = step(H, y)
+        loss_host.copy_(loss, non_blocking=True)
+    barrier()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        H.copy_(H_host, non_blocking=True)
+        y.copy_(y_host, non_blocking=True)
+        loss, _ = step(H, y)
+        loss_host.copy_(loss, non_blocking=True)
+    ev1.record(stream)
+    barrier()
+    ms_e2e = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e = {"value": N * world * args.steps / (ms_e2e * 1e-3), "unit": UNIT,
+           "h2d_bytes_per_step": H_host.numel() * 2 + y_host.numel() * 8, "d2h_bytes_per_step": 4,
+           "loss_last_step": float(loss_host.item())}
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peaks, peak_src = load_peaks()
+    flops_step = 6.0 * N * V * d
+    tflops = flops_step * args.steps / (ms * 1e-3) / 1e12
+    # dominant kernel of the timed region
+    gemm_kinds = {"logits_stats", "logits_grad", "gemm_dH", "gemm_dW"}
+    dom = max(prof, key=lambda k: prof[k]["ms"])
+    p = prof[dom]
+    per_launch_ms = p["ms"] / max(1, p["launches"])
+    per_launch_work = p["work"] / max(1, p["launches"])
+    if dom in gemm_kinds:
+        achieved = per_launch_work / (per_launch_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "peak_source": f"bf16_tflops_sustained ({peak_src})",
+                "work_per_launch": per_launch_work, "work_unit": "flop (2*C*V*d)",
+                "ms_per_launch": per_launch_ms}
+    else:
+        achieved = per_launch_work / (per_launch_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "peak_source": f"hbm_gbs ({peak_src})",
+                "work_per_launch": per_launch_work, "work_unit": "bytes", "ms_per_launch": per_launch_ms}
+    roof["traffic"] = traffic_for(dom)
+    total_ms = sum(v["ms"] for v in prof.values())
+    kernels = {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
+                   "share": round(v["ms"] / total_ms, 4) if total_ms else 0.0}
+               for k, v in prof.items() if v["launches"]}
+    gpu_launches = sum(v["launches"] for k, v in prof.items() if k != "other")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(w, chunk, args),
+        "tflops": tflops, "pct_of_bf16_peak": tflops / peaks["bf16_tflops"],
+        "pct_of_bf16_peak_sustained": tflops / peaks["bf16_tflops_sustained"],
+        "peak_source": peak_src, "flops_per_step": flops_step,
+        "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches, "e2e": e2e, "clocks": clk,
+        "extra_device_bytes": int(ws.numel()), "unfused_logits_bytes": N * V * 4,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def traffic_for(kernel: str):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary, if it
+    was taken on the kernels as they are now (same source stamp), else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        from chunked_lm_head_linear_gb300 import build
+        with open(path) as f:
+            d = json.load(f)
+        if d.get("source_stamp") != build.source_stamp():
+            return None
+        return d.get("per_launch_bytes", {}).get(kernel)
+    except Exception:
+        return None
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,486 @@
+// C ABI of liblce.so (declared in include/lce.h): argument checks, workspace
+// carve-up, TMA tensor maps and the stream-ordered launch sequence of the
+// chunked LM-head cross-entropy. No device memory is allocated here; every
+// launch goes to the caller's stream and nothing synchronises the host unless
+// the caller asks for it (opts->sync_check).
+//
+// Launch sequence per call ("XTuner on Ascend 910C: Qwen3.5-2B training
+// optimisation", section 3.1.4; tokens in chunks as in "XTuner V1
+// introduction", memory optimisation section):
+//   prepare                      label scan -> n, g/n, range-error bit
+//   for each chunk of C tokens:
+//     logits GEMM (FWD_STATS)    z tiles -> per-tile (max, sum-exp), z_{i,y_i}
+//     combine                    lse_i, loss_i
+//     logits GEMM (FWD_GRAD)     gradient tile G (bf16, [C, V]) from lse     (backward)
+//     dH GEMM                    dH_c = G_c W                                (backward)
+//     dW GEMM                    dW (+)= G_c^T H_c                           (backward)
+//   finalize                     loss = sum_i loss_i / n
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/lce.h"
+#include "lce_internal.h"
+
+namespace {
+
+using lce::DevStatus;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn g_encode = nullptr;
+std::once_flag g_encode_once;
+
+EncodeTiledFn encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+  });
+  return g_encode;
+}
+
+constexpr int64_t kDefaultChunk = 4096;
+constexpr int64_t kVocabTile = lce::kTileN;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+  int64_t C = 0;     // tokens per chunk
+  int64_t T = 0;     // vocabulary tiles per row
+  int64_t ldp = 0;   // row stride (elements) of the gradient tile buffer
+  size_t status = 0, loss_i = 0, lse = 0, ztgt = 0, partials = 0, P = 0, total = 0;
+};
+
+int64_t chunk_of(int64_t N, const lce_opts* o) {
+  int64_t C = (o && o->chunk_tokens > 0) ? o->chunk_tokens : kDefaultChunk;
+  if (C > N) C = N;
+  if (C < 1) C = 1;
+  return C;
+}
+
+Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
+  (void)d;
+  Layout L;
+  L.C = chunk_of(N, o);
+  L.T = ceil_div(V, kVocabTile);
+  L.ldp = ceil_div(V, kVocabTile) * kVocabTile;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  L.status = take(sizeof(DevStatus));
+  const bool fwd = op == LCE_OP_FORWARD || op == LCE_OP_FWD_BWD;
+  const bool bwd = op == LCE_OP_BACKWARD || op == LCE_OP_FWD_BWD;
+  if (fwd) {
+    L.loss_i = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+    L.ztgt = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.partials = take(sizeof(float) * 2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.T));
+  }
+  if (op == LCE_OP_FWD_BWD) L.lse = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+  if (bwd) L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
+  L.total = off;
+  return L;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int check_sizes(int64_t N, int64_t d, int64_t V, const lce_opts* o) {
+  if (N < 0 || d <= 0 || V <= 0 || (d % 8) != 0) return LCE_ERR_INVALID_ARG;
+  if (N > (int64_t{1} << 31) - 1 || V > (int64_t{1} << 31) - 1 || d > (int64_t{1} << 24)) return LCE_ERR_INVALID_ARG;
+  if (o) {
+    if (o->reduction != LCE_MEAN && o->reduction != LCE_SUM) return LCE_ERR_INVALID_ARG;
+    if (o->chunk_tokens < 0 || o->reserved != 0) return LCE_ERR_INVALID_ARG;
+    if (o->accumulate_dW != 0 && o->accumulate_dW != 1) return LCE_ERR_INVALID_ARG;
+  }
+  return LCE_OK;
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+};
+
+int device_check(DeviceInfo* info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LCE_ERR_CUDA;
+  int major = 0, minor = 0, sms = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return LCE_ERR_CUDA;
+  if (major != 10 || minor != 3) return LCE_ERR_UNSUPPORTED_DEVICE;
+  if (encode_fn() == nullptr) return LCE_ERR_CUDA;
+  info->num_sms = sms;
+  return LCE_OK;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride ld
+// (elements), 128-byte swizzle, box = {64 columns, box_rows rows}. Reads past
+// rows/cols return zeros.
+int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? LCE_OK : LCE_ERR_CUDA;
+}
+
+#define LCE_TRY(x)                         \
+  do {                                     \
+    const int _rc = (x);                   \
+    if (_rc != LCE_OK) return _rc;         \
+  } while (0)
+#define LCE_CUDA(x)                                  \
+  do {                                               \
+    if ((x) != cudaSuccess) return LCE_ERR_CUDA;     \
+  } while (0)
+
+// ---------------------------------------------------------------------------
+// Measurement hook: events around each launch while profiling is on.
+// ---------------------------------------------------------------------------
+enum Kind : int {
+  K_PREPARE = 0,
+  K_LOGITS_STATS = 1,
+  K_COMBINE = 2,
+  K_LOGITS_GRAD = 3,
+  K_GEMM_DH = 4,
+  K_GEMM_DW = 5,
+  K_FINALIZE = 6,
+  K_OTHER = 7,
+};
+const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare", "logits_stats", "combine", "logits_grad",
+                                                  "gemm_dH", "gemm_dW", "finalize", "other"};
+
+struct ProfRecord {
+  int kind;
+  cudaEvent_t start, stop;
+  double work;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;
+  std::vector<ProfRecord> recs;
+};
+Profiler g_prof;
+
+cudaEvent_t take_event() {
+  if (!g_prof.pool.empty()) {
+    cudaEvent_t e = g_prof.pool.back();
+    g_prof.pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Run one launch; while profiling, bracket it with events on stream s.
+template <class F>
+int timed(cudaStream_t s, int kind, double work, F&& launch) {
+  if (!g_prof.on) return launch();
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  cudaEvent_t a = take_event(), b = take_event();
+  if (!a || !b) return LCE_ERR_CUDA;
+  if (cudaEventRecord(a, s) != cudaSuccess) return LCE_ERR_CUDA;
+  const int rc = launch();
+  if (cudaEventRecord(b, s) != cudaSuccess) return LCE_ERR_CUDA;
+  g_prof.recs.push_back({kind, a, b, work});
+  return rc;
+}
+
+int cuda_rc(cudaError_t e) { return e == cudaSuccess ? LCE_OK : LCE_ERR_CUDA; }
+
+struct Call {
+  const uint16_t* H;
+  const uint16_t* W;
+  const int64_t* y;
+  int64_t N, d, V;
+  lce_opts o;
+  uint8_t* ws;
+  Layout L;
+  DevStatus* st;
+  cudaStream_t s;
+  DeviceInfo dev;
+};
+
+// Logits GEMM for one chunk, in one of the FwdMode epilogues.
+int logits_gemm(const Call& c, int64_t c0, int64_t rows, int mode, float* lse_rows, uint16_t* P) {
+  CUtensorMap mA, mB;
+  LCE_TRY(make_map(&mA, c.H + c0 * c.d, rows, c.d, c.d, lce::kTileM));
+  LCE_TRY(make_map(&mB, c.W, c.V, c.d, c.d, lce::kTileN));
+  lce::GemmGeomHost g{static_cast<int>(ceil_div(rows, lce::kTileM)), static_cast<int>(c.L.T),
+                      static_cast<int>(ceil_div(c.d, lce::kTileK)), 1};
+  lce::FwdParams p;
+  std::memset(&p, 0, sizeof p);
+  p.mode = mode;
+  p.rows = static_cast<int>(rows);
+  p.V = static_cast<int>(c.V);
+  p.ntiles_v = static_cast<int>(c.L.T);
+  p.ignore_index = c.o.ignore_index;
+  p.y = c.y + c0;
+  p.partials = reinterpret_cast<float2*>(c.ws + c.L.partials);
+  p.ztgt = reinterpret_cast<float*>(c.ws + c.L.ztgt);
+  p.lse = lse_rows;
+  p.P = reinterpret_cast<__nv_bfloat16*>(P);
+  p.ldp = c.L.ldp;
+  p.flags = &c.st->flags;
+  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
+  return timed(c.s, mode == lce::FWD_GRAD ? K_LOGITS_GRAD : K_LOGITS_STATS, flops,
+               [&] { return cuda_rc(lce::launch_fwd_gemm(mA, mB, g, p, c.dev.num_sms, c.s)); });
+}
+
+int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* loss_i) {
+  LCE_TRY(logits_gemm(c, c0, rows, lce::FWD_STATS, nullptr, nullptr));
+  const double bytes = static_cast<double>(rows) * (8.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4);
+  return timed(c.s, K_COMBINE, bytes, [&] {
+    return cuda_rc(lce::launch_combine(reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(c.L.T),
+                                       static_cast<int>(rows), reinterpret_cast<const float*>(c.ws + c.L.ztgt),
+                                       c.y + c0, static_cast<int>(c.V), c.o.ignore_index, lse + c0, loss_i + c0,
+                                       c.s));
+  });
+}
+
+int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, uint16_t* dH, float* dW,
+                   bool accumulate) {
+  uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
+  LCE_TRY(logits_gemm(c, c0, rows, lce::FWD_GRAD, const_cast<float*>(lse + c0), P));
+
+  // dH_c = G_c W : A = G_c [rows, V] K-major, B = W [V, d] read N-major.
+  CUtensorMap mG, mW;
+  LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kTileM));
+  LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, 64));
+  lce::GemmGeomHost gh{static_cast<int>(ceil_div(rows, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
+                       static_cast<int>(ceil_div(c.V, lce::kTileK)), 0};
+  lce::DhParams dp;
+  dp.rows = static_cast<int>(rows);
+  dp.N = static_cast<int>(c.d);
+  dp.out = reinterpret_cast<__nv_bfloat16*>(dH + c0 * c.d);
+  dp.ld = c.d;
+  dp.rowscale = nullptr;
+  dp.st = c.st;
+  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
+  LCE_TRY(timed(c.s, K_GEMM_DH, flops,
+                [&] { return cuda_rc(lce::launch_dh_gemm(mG, mW, gh, dp, &c.st->flags, c.dev.num_sms, c.s)); }));
+
+  // dW (+)= G_c^T H_c : A = G_c^T (G_c read M-major), B = H_c [rows, d] read N-major.
+  CUtensorMap mGt, mH;
+  LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, 64));
+  LCE_TRY(make_map(&mH, c.H + c0 * c.d, rows, c.d, c.d, 64));
+  lce::GemmGeomHost gw{static_cast<int>(ceil_div(c.V, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
+                       static_cast<int>(ceil_div(rows, lce::kTileK)), 0};
+  lce::DwParams wp;
+  wp.rows = static_cast<int>(c.V);
+  wp.N = static_cast<int>(c.d);
+  wp.out = dW;
+  wp.ld = c.d;
+  wp.accumulate = accumulate ? 1 : 0;
+  wp.st = c.st;
+  return timed(c.s, K_GEMM_DW, flops,
+               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mH, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
+}
+
+int prepare(const Call& c, const float* grad_loss) {
+  return timed(c.s, K_PREPARE, 8.0 * static_cast<double>(c.N), [&] {
+    return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V), c.o.ignore_index, c.o.reduction,
+                                       c.o.n_valid_override, grad_loss, c.st, c.s));
+  });
+}
+
+int finalize(const Call& c, const float* loss_i, float* loss) {
+  return timed(c.s, K_FINALIZE, 4.0 * static_cast<double>(c.N),
+               [&] { return cuda_rc(lce::launch_finalize(loss_i, c.N, c.st, loss, c.s)); });
+}
+
+int finish(const Call& c) {
+  if (!c.o.sync_check) return LCE_OK;
+  LCE_CUDA(cudaStreamSynchronize(c.s));
+  int flags = 0;
+  LCE_CUDA(cudaMemcpy(&flags, &c.st->flags, sizeof flags, cudaMemcpyDeviceToHost));
+  if (flags & lce::kFlagTimeout) return LCE_ERR_TIMEOUT;
+  if (flags & lce::kFlagLabelRange) return LCE_ERR_LABEL_RANGE;
+  return LCE_OK;
+}
+
+int begin(Call* c, int op, const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+          const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  lce_opts_init(&c->o);
+  if (opts) c->o = *opts;
+  LCE_TRY(check_sizes(N, d, V, &c->o));
+  if (!W || !ws || (N > 0 && (!H || !y))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(W, 16) || (H && !aligned(H, 16)) || (y && !aligned(y, 16)) || !aligned(ws, 256))
+    return LCE_ERR_ALIGNMENT;
+  c->L = make_layout(op, N, d, V, &c->o);
+  if (ws_bytes < c->L.total) return LCE_ERR_WORKSPACE;
+  c->H = static_cast<const uint16_t*>(H);
+  c->W = static_cast<const uint16_t*>(W);
+  c->y = y;
+  c->N = N;
+  c->d = d;
+  c->V = V;
+  c->ws = static_cast<uint8_t*>(ws);
+  c->st = reinterpret_cast<DevStatus*>(c->ws + c->L.status);
+  c->s = static_cast<cudaStream_t>(stream);
+  return LCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void lce_opts_init(lce_opts* o) {
+  if (!o) return;
+  std::memset(o, 0, sizeof *o);
+  o->chunk_tokens = 0;
+  o->ignore_index = -100;
+  o->n_valid_override = -1;
+  o->reduction = LCE_MEAN;
+}
+
+size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opts* opts) {
+  lce_opts o;
+  lce_opts_init(&o);
+  if (opts) o = *opts;
+  if (op < LCE_OP_FORWARD || op > LCE_OP_FWD_BWD) return 0;
+  if (check_sizes(N, d, V, &o) != LCE_OK) return 0;
+  return make_layout(op, N, d, V, &o).total;
+}
+
+int lce_forward(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V, float* loss,
+                float* lse, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  Call c;
+  LCE_TRY(begin(&c, LCE_OP_FORWARD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
+  if (!loss || (N > 0 && !lse)) return LCE_ERR_INVALID_ARG;
+  if (!aligned(loss, 4) || (lse && !aligned(lse, 16))) return LCE_ERR_ALIGNMENT;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, nullptr));
+  float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
+  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+    const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    LCE_TRY(forward_chunk(c, c0, rows, lse, loss_i));
+  }
+  LCE_TRY(finalize(c, loss_i, loss));
+  return finish(c);
+}
+
+int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V, const float* lse,
+                 const float* grad_loss, void* dH, float* dW, const lce_opts* opts, void* ws, size_t ws_bytes,
+                 void* stream) {
+  Call c;
+  LCE_TRY(begin(&c, LCE_OP_BACKWARD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
+  if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
+      (grad_loss && !aligned(grad_loss, 4)))
+    return LCE_ERR_ALIGNMENT;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, grad_loss));
+  if (N == 0 && !c.o.accumulate_dW)
+    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
+                  [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
+  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+    const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    LCE_TRY(backward_chunk(c, c0, rows, lse, static_cast<uint16_t*>(dH), dW, c.o.accumulate_dW || c0 > 0));
+  }
+  return finish(c);
+}
+
+int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts, void* ws,
+                size_t ws_bytes, void* stream) {
+  Call c;
+  LCE_TRY(begin(&c, LCE_OP_FWD_BWD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
+  if (!loss || !dW || (N > 0 && !dH)) return LCE_ERR_INVALID_ARG;
+  if (!aligned(loss, 4) || !aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
+      (grad_loss && !aligned(grad_loss, 4)))
+    return LCE_ERR_ALIGNMENT;
+  LCE_TRY(device_check(&c.dev));
+  float* lse_rows = lse ? lse : reinterpret_cast<float*>(c.ws + c.L.lse);
+  float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
+  LCE_TRY(prepare(c, grad_loss));
+  if (N == 0 && !c.o.accumulate_dW)
+    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
+                  [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
+  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+    const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    LCE_TRY(forward_chunk(c, c0, rows, lse_rows, loss_i));
+    LCE_TRY(backward_chunk(c, c0, rows, lse_rows, static_cast<uint16_t*>(dH), dW, c.o.accumulate_dW || c0 > 0));
+  }
+  LCE_TRY(finalize(c, loss_i, loss));
+  return finish(c);
+}
+
+int lce_read_device_status(const void* ws, void* stream, int* flags) {
+  if (!ws || !flags) return LCE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256)) return LCE_ERR_ALIGNMENT;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LCE_ERR_CUDA;
+  int f = 0;
+  if (cudaMemcpy(&f, ws, sizeof f, cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
+  *flags = f & (LCE_DEVICE_LABEL_RANGE | LCE_DEVICE_TIMEOUT);
+  return LCE_OK;
+}
+
+const char* lce_status_string(int status) {
+  switch (status) {
+    case LCE_OK: return "ok";
+    case LCE_ERR_INVALID_ARG: return "invalid argument";
+    case LCE_ERR_ALIGNMENT: return "misaligned pointer";
+    case LCE_ERR_WORKSPACE: return "workspace too small";
+    case LCE_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+    case LCE_ERR_CUDA: return "CUDA error";
+    case LCE_ERR_LABEL_RANGE: return "label outside [0, V) and not ignore_index";
+    case LCE_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int lce_version(void) { return LCE_VERSION; }
+
+int lce_profile_begin(void) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.recs.clear();
+  g_prof.on = true;
+  return LCE_OK;
+}
+
+int lce_profile_end(lce_profile* out) {
+  std::lock_guard<std::mutex> lock(g_prof.mu);
+  g_prof.on = false;
+  lce_profile p;
+  std::memset(&p, 0, sizeof p);
+  int rc = LCE_OK;
+  for (const ProfRecord& r : g_prof.recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      rc = LCE_ERR_CUDA;
+    p.launches[r.kind] += 1;
+    p.ms[r.kind] += ms;
+    p.work[r.kind] += r.work;
+    g_prof.pool.push_back(r.start);
+    g_prof.pool.push_back(r.stop);
+  }
+  g_prof.recs.clear();
+  if (out) *out = p;
+  return rc;
+}
+
+const char* lce_kernel_name(int kind) {
+  return (kind >= 0 && kind < LCE_KERNEL_KINDS) ? kKindNames[kind] : nullptr;
+}
+
+}  // extern "C"

@@ -1,0 +1,254 @@
+// Persistent, warp-specialised tcgen05 GEMM core shared by the three
+// contractions of the fused LM-head cross-entropy:
+//
+//   logits   z_c  = H_c W^T        A = H_c   [C, d] K-major,  B = W   [V, d] K-major
+//   input    dH_c = G_c W          A = G_c   [C, V] K-major,  B = W   [V, d] MN-major
+//   weight   dW  += G_c^T H_c      A = G_c^T (G_c MN-major), B = H_c [C, d] MN-major
+//
+// ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation", section 3.1.4:
+// the logits chunk, and the backward's d_input / d_weight.)
+//
+// One CTA per SM, 256 threads:
+//   warp 0     TMA producer (one thread): A/B k-blocks into a STAGES-deep ring
+//   warp 1     MMA issuer (one thread): tcgen05.mma 128x256x16, fp32 in TMEM
+//   warp 2     TMEM allocator (512 columns = two 128x256 fp32 accumulators)
+//   warps 4-7  epilogue: TMEM -> registers -> per-tile arithmetic -> global
+// The two accumulators alternate so the epilogue of tile t overlaps the main
+// loop of tile t+1. Tiles are assigned statically: tile = blockIdx.x + i*grid.
+#pragma once
+
+#include "lce_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace lce {
+
+constexpr int BM = 128;             // rows of an output tile (TMEM lanes)
+constexpr int BN = 256;             // columns of an output tile (TMEM columns)
+constexpr int BK = 64;              // k-block: 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
+constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
+constexpr int MN_SLAB_BYTES = 64 * BK * 2;   // one 64-wide MN slab of a k-block: 8 KiB
+constexpr int NUM_THREADS = 256;
+constexpr int EPI_WARP0 = 4;
+constexpr int TMEM_COLS = 2 * BN;
+
+struct GemmGeom {
+  int m_tiles, n_tiles, k_blocks;
+  int m_fast;        // 1: consecutive tiles walk M first (share the B tile)
+  int* flags;        // device status word (timeout is reported here)
+};
+
+struct SmemLayout {
+  static constexpr int kTiles = STAGES * (A_STAGE_BYTES + B_STAGE_BYTES);
+  static constexpr int kBars = kTiles;                  // mbarriers after the tiles
+  static constexpr int kNumBars = 2 * STAGES + 4 + 1;   // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int kMisc = kBars + kNumBars * 8;    // tmem holder + abort flag
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kDynamicBytes = kTotal + 1024;   // slack for 1 KiB alignment
+};
+
+__device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& m_blk, int& n_blk) {
+  if (g.m_fast) {
+    m_blk = t % g.m_tiles;
+    n_blk = t / g.m_tiles;
+  } else {
+    n_blk = t % g.n_tiles;
+    m_blk = t / g.n_tiles;
+  }
+}
+
+// Broadcast a lane-0 wait result to the warp so every lane takes the same path
+// (the epilogue's tcgen05.ld instructions are warp-collective).
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void report_timeout(volatile int* abort, int* flags) {
+  *abort = 1;
+  atomicOr(flags, kFlagTimeout);
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmGeom g,
+                typename Epi::Params ep) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SmemLayout::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + SmemLayout::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int num_tiles = g.m_tiles * g.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0;             // bit s: stage s has a load in flight we armed
+    uint32_t armed_parity = 0;      // bit s: parity of that load's phase
+    bool ok = true;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      int mb, nb;
+      tile_coords(g, t, mb, nb);
+      const int m0 = mb * BM, n0 = nb * BN;
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
+          report_timeout(abort, g.flags);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
+        const int k0 = kb * BK;
+        uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
+        uint8_t* b_dst = sB + stage * B_STAGE_BYTES;
+        if (A_MN) {
+#pragma unroll
+          for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * MN_SLAB_BYTES, &tmA, &full[stage], m0 + 64 * j, k0);
+        } else {
+          tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
+        }
+        if (B_MN) {
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * MN_SLAB_BYTES, &tmB, &full[stage], n0 + 64 * j, k0);
+        } else {
+          tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
+        }
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok || *abort) {
+      // Leave no copy in flight: wait (briefly) for every load this thread armed.
+      for (int s = 0; s < STAGES; ++s)
+        if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u, 100000000ull);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued = false;
+    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort)) {
+        report_timeout(abort, g.flags);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort)) {
+          report_timeout(abort, g.flags);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          // K-major: the next 16 elements are 32 bytes further along the row.
+          // MN-major: the next 16 K rows are 16 * 128 bytes further.
+          const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + k * 2048, MN_SLAB_BYTES, 1024)
+                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + k * 2048, MN_SLAB_BYTES, 1024)
+                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        issued = true;
+        umma_commit(&empty[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit(&tfull[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (*abort && issued) {
+      // Make sure no MMA still writes TMEM before it is released.
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, 100000000ull);
+    }
+  } else if (warp >= EPI_WARP0) {
+    // ---------------- epilogue ----------------
+    const int q = warp - EPI_WARP0;   // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;    // row of the output tile
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    typename Epi::State st;
+    Epi::init(ep, st);
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+      if (!warp_wait(&tfull[acc], acc_phase, abort, lane)) {
+        if (lane == 0) report_timeout(abort, g.flags);
+        break;
+      }
+      tc_fence_after_sync();
+      int mb, nb;
+      tile_coords(g, t, mb, nb);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      Epi::tile(ep, st, mb * BM, nb * BN, row, taddr);
+      tc_fence_before_sync();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+}  // namespace lce

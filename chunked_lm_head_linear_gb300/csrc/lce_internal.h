@@ -1,0 +1,91 @@
+// Internal interface between the C-ABI layer (lce_api.cu) and the kernels
+// (lce_kernels.cu). Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace lce {
+
+// Device status bits (the workspace's flag word; the first two equal the
+// public LCE_DEVICE_* bits).
+constexpr int kFlagLabelRange = 1;
+constexpr int kFlagTimeout = 2;
+
+// Device-side status block at the start of the workspace.
+struct DevStatus {
+  int flags;              // kFlag* bits
+  int pad0;
+  long long n_valid;      // denominator n actually used (count or override)
+  long long n_counted;    // valid labels counted in this call
+  float gscale;           // g / n (mean), g (sum); 0 when n == 0 under mean
+  float pad1;
+  double lscale;          // 1 / n (mean), 1 (sum); 0 when n == 0 under mean
+};
+
+enum FwdMode : int {
+  FWD_STATS = 0,    // per-(row, vocab tile) max / sum-exp partials + target logit
+  FWD_GRAD = 2,     // gradient tile exp(z - lse) - onehot (valid rows), from a known lse
+  FWD_REF = 3,      // row maximum over the first vocabulary tile
+};
+
+struct FwdParams {
+  int mode;
+  int rows;              // rows of this chunk
+  int V;
+  int ntiles_v;          // vocabulary tiles per row (partials row stride)
+  long long ignore_index;
+  const int64_t* y;      // labels of this chunk
+  float2* partials;      // [rows, ntiles_v] (max, sum-exp)
+  float* ztgt;           // [rows] logit of the label
+  float* ref;            // [rows] row reference (FWD_REF output)
+  const float* lse;      // [rows] (FWD_GRAD input)
+  __nv_bfloat16* P;      // [rows, ldp] gradient tile output (FWD_GRAD)
+  long long ldp;
+  int* flags;
+};
+
+struct DhParams {
+  int rows;              // rows of this chunk
+  int N;                 // d
+  __nv_bfloat16* out;    // dH of this chunk, [rows, ld]
+  long long ld;
+  const float* rowscale; // optional per-row factor (nullptr: none)
+  const DevStatus* st;   // gscale
+};
+
+struct DwParams {
+  int rows;              // V
+  int N;                 // d
+  float* out;            // dW [V, ld]
+  long long ld;
+  int accumulate;        // 1: out += result
+  const DevStatus* st;   // gscale
+};
+
+struct GemmGeomHost {
+  int m_tiles, n_tiles, k_blocks, m_fast;
+};
+
+// Kernel launches (return cudaGetLastError()).
+cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
+                           long long n_override, const float* grad_loss, DevStatus* st, cudaStream_t s);
+cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+                            const FwdParams& p, int num_sms, cudaStream_t s);
+cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+                           const DhParams& p, int* flags, int num_sms, cudaStream_t s);
+cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+                           const DwParams& p, int* flags, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+                           int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
+cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
+
+// GEMM tile geometry (must match the kernels).
+constexpr int kTileM = 128;
+constexpr int kTileN = 256;
+constexpr int kTileK = 64;
+int gemm_smem_bytes();
+
+}  // namespace lce

@@ -1,0 +1,347 @@
+// Kernels of the fused LM-head linear + cross-entropy: the three tcgen05
+// GEMM instantiations with their epilogues, and the small per-row kernels.
+//
+// Where the arithmetic comes from:
+//   * token-level cross-entropy over the vocabulary of H W^T, its d_input and
+//     d_weight ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation",
+//     section 3.1.4, Fig. 12: the fused backward emits d_weight / d_input and
+//     never stores the full d_logits);
+//   * the streaming max / sum-exp over vocabulary tiles ("MindSpeed fusion
+//     optimisation: principles and practice", section 3.2: blockwise softmax
+//     without materialising the full score matrix), applied here along the
+//     vocabulary instead of the attention keys.
+#include <math.h>
+
+#include "lce_gemm.cuh"
+#include "lce_internal.h"
+
+namespace lce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ----------------------------------------------------------------------------
+// Logits epilogue. Each thread owns one row of the 128 x 256 tile.
+//   FWD_STATS: per (row, vocab tile) running max m and sum of exp(z - m) over
+//              the tile's in-vocabulary columns, plus the label's logit.
+//   FWD_REF:   the row maximum over the tile (launched for tile 0 only).
+//   FWD_GRAD:  the gradient tile exp(z - lse) - [v = y] in bf16 for valid rows,
+//              zeros for ignored rows and for columns past the vocabulary.
+// ----------------------------------------------------------------------------
+struct FwdEpi {
+  using Params = FwdParams;
+  struct State {};
+  static __device__ __forceinline__ void init(const Params&, State&) {}
+
+  static __device__ __forceinline__ void tile(const Params& p, State&, int m0, int n0, int row, uint32_t taddr) {
+    const int r = m0 + row;
+    const bool live = r < p.rows;
+    const long long yr = live ? static_cast<long long>(p.y[r]) : p.ignore_index;
+    const bool valid = live && yr != p.ignore_index && yr >= 0 && yr < p.V;
+    const int ycol = valid ? static_cast<int>(yr - n0) : -1;
+    const int vlim = p.V - n0;  // columns >= vlim are past the vocabulary
+
+    if (p.mode == FWD_GRAD) {
+      grad_tile(p, r, live, valid, ycol, vlim, n0, taddr);
+      return;
+    }
+    float m = -INFINITY, s = 0.f, zt = 0.f;
+    bool have_t = false;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      float v[32];
+      tmem_ld_32x32b_x32(taddr + j * 32, v);
+      const int c0 = j * 32;
+      float cm = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 32; ++c)
+        if (c0 + c < vlim) cm = fmaxf(cm, v[c]);
+      if (p.mode == FWD_STATS) {
+        if (cm > m) {
+          s *= exp2f((m - cm) * kLog2e);
+          m = cm;
+        }
+        const float mb = m * kLog2e;
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c0 + c < vlim) s += exp2f(fmaf(v[c], kLog2e, -mb));
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          if (c0 + c == ycol) {
+            zt = v[c];
+            have_t = true;
+          }
+      } else {
+        m = fmaxf(m, cm);
+      }
+    }
+    if (!live) return;
+    if (p.mode == FWD_STATS) {
+      p.partials[static_cast<long long>(r) * p.ntiles_v + n0 / BN] = make_float2(m, s);
+      if (have_t) p.ztgt[r] = zt;
+    } else {
+      p.ref[r] = m;
+    }
+  }
+
+  static __device__ __forceinline__ void grad_tile(const Params& p, int r, bool live, bool valid, int ycol, int vlim,
+                                                   int n0, uint32_t taddr) {
+    const float rb = (live ? p.lse[r] : 0.f) * kLog2e;
+    __nv_bfloat16* dst = p.P + static_cast<long long>(r) * p.ldp + n0;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      float v[32];
+      tmem_ld_32x32b_x32(taddr + j * 32, v);
+      if (!live) continue;
+      const int c0 = j * 32;
+      uint32_t pk[16];
+#pragma unroll
+      for (int c = 0; c < 32; c += 2) {
+        float e0 = 0.f, e1 = 0.f;
+        if (valid) {
+          if (c0 + c < vlim) e0 = exp2f(fmaf(v[c], kLog2e, -rb)) - (c0 + c == ycol ? 1.f : 0.f);
+          if (c0 + c + 1 < vlim) e1 = exp2f(fmaf(v[c + 1], kLog2e, -rb)) - (c0 + c + 1 == ycol ? 1.f : 0.f);
+        }
+        pk[c / 2] = pack_bf16x2(e0, e1);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+};
+
+// dH tile: bf16(acc * g/n [* per-row factor]) into the chunk's rows of dH.
+struct DhEpi {
+  using Params = DhParams;
+  struct State {
+    float g;
+  };
+  static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
+    const int r = m0 + row;
+    const bool live = r < p.rows;
+    float f = st.g;
+    if (live && p.rowscale != nullptr) f *= p.rowscale[r];
+    __nv_bfloat16* dst = p.out + static_cast<long long>(r) * p.ld + n0;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      float v[32];
+      tmem_ld_32x32b_x32(taddr + j * 32, v);
+      if (!live) continue;
+      const int c0 = j * 32;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (n0 + c0 + 8 * q < p.N) {
+          uint4 w;
+          w.x = pack_bf16x2(v[8 * q + 0] * f, v[8 * q + 1] * f);
+          w.y = pack_bf16x2(v[8 * q + 2] * f, v[8 * q + 3] * f);
+          w.z = pack_bf16x2(v[8 * q + 4] * f, v[8 * q + 5] * f);
+          w.w = pack_bf16x2(v[8 * q + 6] * f, v[8 * q + 7] * f);
+          *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = w;
+        }
+      }
+    }
+  }
+};
+
+// dW tile: fp32 (acc * g/n) stored into, or added to, the vocabulary rows of dW.
+struct DwEpi {
+  using Params = DwParams;
+  struct State {
+    float g;
+  };
+  static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
+
+  static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
+    const int r = m0 + row;
+    const bool live = r < p.rows;
+    const float f = st.g;
+    float* dst = p.out + static_cast<long long>(r) * p.ld + n0;
+#pragma unroll 1
+    for (int j = 0; j < BN / 32; ++j) {
+      float v[32];
+      tmem_ld_32x32b_x32(taddr + j * 32, v);
+      if (!live) continue;
+      const int c0 = j * 32;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (n0 + c0 + 4 * q < p.N) {
+          float4* a = reinterpret_cast<float4*>(dst + c0 + 4 * q);
+          float4 o = p.accumulate ? *a : make_float4(0.f, 0.f, 0.f, 0.f);
+          o.x += v[4 * q + 0] * f;
+          o.y += v[4 * q + 1] * f;
+          o.z += v[4 * q + 2] * f;
+          o.w += v[4 * q + 3] * f;
+          *a = o;
+        }
+      }
+    }
+  }
+};
+
+// ----------------------------------------------------------------------------
+// Label scan: n = number of labels in [0, V) that are not ignore_index, the
+// range-error bit, and the scales g/n and 1/n. One block, fixed-order sums.
+// ----------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_prepare(const int64_t* __restrict__ y, long long N, int V,
+                                                  long long ignore_index, int reduction, long long n_override,
+                                                  const float* grad_loss, DevStatus* st) {
+  __shared__ long long s_cnt[32];
+  __shared__ int s_bad[32];
+  long long cnt = 0;
+  int bad = 0;
+  for (long long i = threadIdx.x; i < N; i += blockDim.x) {
+    const long long v = y[i];
+    if (v != ignore_index) {
+      if (v >= 0 && v < V)
+        ++cnt;
+      else
+        bad = 1;
+    }
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+    bad |= __shfl_xor_sync(0xffffffffu, bad, off);
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    s_cnt[w] = cnt;
+    s_bad[w] = bad;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    long long total = 0;
+    int anybad = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) {
+      total += s_cnt[i];
+      anybad |= s_bad[i];
+    }
+    const long long n = n_override >= 0 ? n_override : total;
+    const float g = grad_loss != nullptr ? *grad_loss : 1.f;
+    st->flags = anybad ? kFlagLabelRange : 0;
+    st->n_counted = total;
+    st->n_valid = n;
+    if (reduction == 0) {
+      st->gscale = n > 0 ? g / static_cast<float>(n) : 0.f;
+      st->lscale = n > 0 ? 1.0 / static_cast<double>(n) : 0.0;
+    } else {
+      st->gscale = g;
+      st->lscale = 1.0;
+    }
+  }
+}
+
+// Merge two (max, sum-exp) pairs: m' = max, s' = s1 e^{m1-m'} + s2 e^{m2-m'}.
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+  const float M = fmaxf(m, m2);
+  const float e1 = (m == M) ? 1.f : exp2f((m - M) * kLog2e);
+  const float e2 = (m2 == M) ? 1.f : exp2f((m2 - M) * kLog2e);
+  s = s * e1 + s2 * e2;
+  m = M;
+}
+
+// One warp per row: combine the row's vocabulary-tile partials in a fixed
+// order, lse = m + log s, loss_i = lse - z_y for valid rows (else 0).
+__global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ partials, int T, int rows,
+                                                 const float* __restrict__ ztgt, const int64_t* __restrict__ y,
+                                                 int V, long long ignore_index, float* __restrict__ lse,
+                                                 float* __restrict__ loss_i) {
+  const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float m = -INFINITY, s = 0.f;
+  const float2* pr = partials + static_cast<long long>(r) * T;
+  for (int t = lane; t < T; t += 32) {
+    const float2 q = pr[t];
+    merge_ms(m, s, q.x, q.y);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_ms(m, s, m2, s2);
+  }
+  if (lane == 0) {
+    const float l = m + logf(s);
+    lse[r] = l;
+    const long long yr = y[r];
+    const bool valid = yr != ignore_index && yr >= 0 && yr < V;
+    loss_i[r] = valid ? l - ztgt[r] : 0.f;
+  }
+}
+
+// loss = (sum_i loss_i) * lscale, fp64 accumulation in a fixed order.
+__global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ loss_i, long long N,
+                                                   const DevStatus* st, float* loss) {
+  __shared__ double red[1024];
+  double acc = 0.0;
+  for (long long i = threadIdx.x; i < N; i += blockDim.x) acc += static_cast<double>(loss_i[i]);
+  red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (static_cast<int>(threadIdx.x) < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = static_cast<float>(red[0] * st->lscale);
+}
+
+// ----------------------------------------------------------------------------
+// Launch wrappers
+// ----------------------------------------------------------------------------
+int gemm_smem_bytes() { return SmemLayout::kDynamicBytes; }
+
+template <bool A_MN, bool B_MN, class Epi>
+static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& gh,
+                               const typename Epi::Params& ep, int* flags, int num_sms, cudaStream_t s) {
+  auto kern = gemm_kernel<A_MN, B_MN, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::kDynamicBytes);
+  if (e != cudaSuccess) return e;
+  GemmGeom g;
+  g.m_tiles = gh.m_tiles;
+  g.n_tiles = gh.n_tiles;
+  g.k_blocks = gh.k_blocks;
+  g.m_fast = gh.m_fast;
+  g.flags = flags;
+  const int tiles = gh.m_tiles * gh.n_tiles;
+  if (tiles <= 0) return cudaSuccess;
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  kern<<<grid, NUM_THREADS, SmemLayout::kDynamicBytes, s>>>(a, b, g, ep);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const FwdParams& p,
+                            int num_sms, cudaStream_t s) {
+  return launch_gemm<false, false, FwdEpi>(a, b, g, p, p.flags, num_sms, s);
+}
+
+cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const DhParams& p,
+                           int* flags, int num_sms, cudaStream_t s) {
+  return launch_gemm<false, true, DhEpi>(a, b, g, p, flags, num_sms, s);
+}
+
+cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const DwParams& p,
+                           int* flags, int num_sms, cudaStream_t s) {
+  return launch_gemm<true, true, DwEpi>(a, b, g, p, flags, num_sms, s);
+}
+
+cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
+                           long long n_override, const float* grad_loss, DevStatus* st, cudaStream_t s) {
+  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+                           int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const int grid = (rows + warps_per_block - 1) / warps_per_block;
+  k_combine<<<grid, 32 * warps_per_block, 0, s>>>(partials, ntiles_v, rows, ztgt, y, V, ignore_index, lse, loss_i);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s) {
+  k_finalize<<<1, 1024, 0, s>>>(loss_i, N, st, loss);
+  return cudaGetLastError();
+}
+
+}  // namespace lce

@@ -1,0 +1,232 @@
+"""Python binding of liblce.so (the C ABI declared in include/lce.h).
+
+Argument marshalling only: PyTorch allocates outputs and the workspace and
+supplies the current CUDA stream; every step of the computation runs in the
+library's CUDA kernels. There is no CPU fallback: if the library is missing,
+``load()`` raises.
+
+Entry points (same names as the C ABI):
+  lce_forward(H, W, y)              -> loss [1], lse [N]
+  lce_backward(H, W, y, lse, g)     -> dH [N, d] bf16, dW [V, d] fp32
+  lce_fwd_bwd(H, W, y, g)           -> loss, lse, dH, dW
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "liblce.so")
+
+LCE_OK = 0
+LCE_ERR_INVALID_ARG = 1
+LCE_ERR_ALIGNMENT = 2
+LCE_ERR_WORKSPACE = 3
+LCE_ERR_UNSUPPORTED_DEVICE = 4
+LCE_ERR_CUDA = 5
+LCE_ERR_LABEL_RANGE = 6
+LCE_ERR_TIMEOUT = 7
+
+LCE_MEAN, LCE_SUM = 0, 1
+LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD = 0, 1, 2
+LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
+
+# Every symbol include/lce.h declares.
+EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
+            "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
+            "lce_profile_end", "lce_kernel_name")
+LCE_KERNEL_KINDS = 8
+
+
+class LceOpts(ctypes.Structure):
+    _fields_ = [("chunk_tokens", ctypes.c_int64), ("ignore_index", ctypes.c_int64),
+                ("n_valid_override", ctypes.c_int64), ("reduction", ctypes.c_int32),
+                ("accumulate_dW", ctypes.c_int32), ("sync_check", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class LceProfile(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int32 * LCE_KERNEL_KINDS), ("ms", ctypes.c_double * LCE_KERNEL_KINDS),
+                ("work", ctypes.c_double * LCE_KERNEL_KINDS)]
+
+
+class LCEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {status_string(code)} (status {code})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load liblce.so (built by ``chunked_lm_head_linear_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"liblce.so not found at {p}: build it with "
+                               "`python -m chunked_lm_head_linear_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(p)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        OPT = ctypes.POINTER(LceOpts)
+        lib.lce_opts_init.argtypes = [OPT]
+        lib.lce_opts_init.restype = None
+        lib.lce_workspace_size.argtypes = [I32, I64, I64, I64, OPT]
+        lib.lce_workspace_size.restype = ctypes.c_size_t
+        lib.lce_forward.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_forward.restype = I32
+        lib.lce_backward.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_backward.restype = I32
+        lib.lce_fwd_bwd.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_fwd_bwd.restype = I32
+        lib.lce_read_device_status.argtypes = [P, P, ctypes.POINTER(I32)]
+        lib.lce_read_device_status.restype = I32
+        lib.lce_status_string.argtypes = [I32]
+        lib.lce_status_string.restype = ctypes.c_char_p
+        lib.lce_version.argtypes = []
+        lib.lce_version.restype = I32
+        lib.lce_profile_begin.argtypes = []
+        lib.lce_profile_begin.restype = I32
+        lib.lce_profile_end.argtypes = [ctypes.POINTER(LceProfile)]
+        lib.lce_profile_end.restype = I32
+        lib.lce_kernel_name.argtypes = [I32]
+        lib.lce_kernel_name.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().lce_status_string(int(code)).decode()
+
+
+def make_opts(chunk_tokens=0, ignore_index=-100, reduction="mean", n_valid_override=-1,
+              accumulate_dW=False, sync_check=False) -> LceOpts:
+    o = LceOpts()
+    load().lce_opts_init(ctypes.byref(o))
+    o.chunk_tokens = int(chunk_tokens)
+    o.ignore_index = int(ignore_index)
+    o.n_valid_override = int(n_valid_override)
+    o.reduction = {"mean": LCE_MEAN, "sum": LCE_SUM}[reduction] if isinstance(reduction, str) else int(reduction)
+    o.accumulate_dW = int(bool(accumulate_dW))
+    o.sync_check = int(bool(sync_check))
+    return o
+
+
+def workspace_size(op: int, N: int, d: int, V: int, opts: LceOpts | None = None) -> int:
+    return int(load().lce_workspace_size(op, N, d, V, ctypes.byref(opts) if opts is not None else None))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_inputs(H, W, y):
+    import torch
+    if not (H.is_cuda and W.is_cuda and y.is_cuda):
+        raise ValueError("H, W and y must be CUDA tensors (there is no CPU path)")
+    if H.dtype != torch.bfloat16 or W.dtype != torch.bfloat16 or y.dtype != torch.int64:
+        raise ValueError("H and W must be bfloat16, y int64")
+    if H.dim() != 2 or W.dim() != 2 or y.dim() != 1 or H.shape[1] != W.shape[1] or y.shape[0] != H.shape[0]:
+        raise ValueError("shapes must be H [N, d], W [V, d], y [N]")
+    if not (H.is_contiguous() and W.is_contiguous() and y.is_contiguous()):
+        raise ValueError("H, W and y must be contiguous")
+    return H.shape[0], H.shape[1], W.shape[0]
+
+
+def _workspace(op, N, d, V, opts, device, workspace=None):
+    import torch
+    need = workspace_size(op, N, d, V, opts)
+    if need == 0:
+        raise LCEError(LCE_ERR_INVALID_ARG, "lce_workspace_size")
+    if workspace is not None and workspace.numel() >= need:
+        return workspace
+    # torch's allocator returns 512-byte aligned blocks
+    return torch.empty(need, dtype=torch.uint8, device=device)
+
+
+def _raise(rc, where):
+    if rc != LCE_OK:
+        raise LCEError(rc, where)
+
+
+def lce_forward(H, W, y, *, workspace=None, stream=None, **opt_kw):
+    """loss (fp32 [1]) and lse (fp32 [N]) of the token-level cross-entropy."""
+    import torch
+    N, d, V = _check_inputs(H, W, y)
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_FORWARD, N, d, V, opts, H.device, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
+    rc = load().lce_forward(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(loss), _ptr(lse), ctypes.byref(opts),
+                            _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_forward")
+    return loss, lse
+
+
+def lce_backward(H, W, y, lse, grad_loss=None, *, dW=None, workspace=None, stream=None, **opt_kw):
+    """dH (bf16 [N, d]) and dW (fp32 [V, d]) from a saved lse; grad_loss is a
+    device fp32 scalar tensor or None (1.0)."""
+    import torch
+    N, d, V = _check_inputs(H, W, y)
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_BACKWARD, N, d, V, opts, H.device, workspace)
+    dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
+    rc = load().lce_backward(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW),
+                             ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_backward")
+    return dH, dW
+
+
+def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, stream=None, **opt_kw):
+    """loss, lse, dH, dW in one call."""
+    import torch
+    N, d, V = _check_inputs(H, W, y)
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_FWD_BWD, N, d, V, opts, H.device, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    if lse is None:
+        lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
+    dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
+    rc = load().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(dH),
+                            _ptr(dW), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_fwd_bwd")
+    return loss, lse, dH, dW
+
+
+def read_device_status(workspace, stream=None) -> int:
+    """Device status bits (LCE_DEVICE_*) left in a workspace by the last call."""
+    flags = ctypes.c_int(0)
+    _raise(load().lce_read_device_status(_ptr(workspace), _stream(stream), ctypes.byref(flags)),
+           "lce_read_device_status")
+    return flags.value
+
+
+def profile_begin():
+    """Start bracketing every library launch with CUDA events on its stream."""
+    _raise(load().lce_profile_begin(), "lce_profile_begin")
+
+
+def profile_end() -> dict:
+    """Stop profiling; per kernel kind: launches, summed device ms, summed work."""
+    p = LceProfile()
+    _raise(load().lce_profile_end(ctypes.byref(p)), "lce_profile_end")
+    out = {}
+    for k in range(LCE_KERNEL_KINDS):
+        name = load().lce_kernel_name(k).decode()
+        out[name] = {"launches": p.launches[k], "ms": p.ms[k], "work": p.work[k]}
+    return out

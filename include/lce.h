@@ -1,0 +1,154 @@
+/*
+ * lce.h -- C ABI of liblce.so: fused, chunked LM-head linear + cross-entropy
+ * (forward and backward) on one GB300 (sm_103a).
+ *
+ * The operation ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation",
+ * section 3.1.4, Liger chunked cross-entropy, Fig. 12 and Fig. 13): the LM-head
+ * logits z = H W^T of an N-token batch over a V-word vocabulary feed a
+ * token-level cross-entropy, and the backward produces d_input (dH) and
+ * d_weight (dW) without ever writing the full [N, V] logits or d_logits to
+ * memory. With valid_i = [y_i != ignore_index], n = sum_i valid_i:
+ *
+ *   lse_i  = log sum_v exp(z_iv)
+ *   loss   = sum_i valid_i (lse_i - z_{i,y_i}) / n        (LCE_MEAN; no /n for LCE_SUM)
+ *   G_iv   = valid_i g (exp(z_iv - lse_i) - [v = y_i]) / n (g = upstream gradient)
+ *   dH     = G W,   dW = G^T H
+ *
+ * Tokens are processed in chunks ("XTuner V1 introduction", memory
+ * optimisation section: the loss graph is computed chunk by chunk), so the
+ * extra device memory is O(chunk * V), never O(N * V).
+ *
+ * Conventions for every entry point
+ *   - Pointers named "device" are CUDA device pointers owned by the caller;
+ *     the library never allocates, frees or keeps them.
+ *   - H [N, d] and W [V, d] are bf16, row-major and contiguous; dH [N, d] is
+ *     bf16; dW [V, d], loss [1], lse [N] are fp32; y [N] is int64. All device
+ *     pointers must be 16-byte aligned and d a multiple of 8.
+ *   - ws / ws_bytes: caller-allocated device workspace of at least
+ *     lce_workspace_size(op, ...) bytes, 256-byte aligned. Its contents on
+ *     entry do not matter; two calls running at the same time need two
+ *     workspaces.
+ *   - stream: a cudaStream_t (passed as void*); NULL is the legacy default
+ *     stream. All device work is ordered on it. No call synchronises the host
+ *     unless opts->sync_check is set.
+ *   - Return value: LCE_OK or an LCE_ERR_* code. Argument errors are detected
+ *     on the host before any launch. Device-detected problems (a label outside
+ *     {ignore_index} U [0, V), a wait that timed out) set bits in the
+ *     workspace's status word; the affected row is then treated as ignored
+ *     (never an out-of-bounds read). They become return codes when
+ *     opts->sync_check is set, or through lce_read_device_status().
+ *   - Thread safety: calls with distinct workspaces may run concurrently.
+ */
+#ifndef LCE_H_
+#define LCE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LCE_VERSION 1
+
+/* status codes */
+#define LCE_OK 0
+#define LCE_ERR_INVALID_ARG 1        /* null pointer, N < 0, d/V <= 0, d % 8 != 0, bad option */
+#define LCE_ERR_ALIGNMENT 2          /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+#define LCE_ERR_WORKSPACE 3          /* ws_bytes smaller than lce_workspace_size() */
+#define LCE_ERR_UNSUPPORTED_DEVICE 4 /* the current device is not an sm_103 GPU */
+#define LCE_ERR_CUDA 5               /* a CUDA runtime / driver call failed */
+#define LCE_ERR_LABEL_RANGE 6        /* a label is neither ignore_index nor in [0, V) */
+#define LCE_ERR_TIMEOUT 7            /* a device-side wait exceeded its limit */
+
+/* reductions */
+#define LCE_MEAN 0
+#define LCE_SUM 1
+
+/* ops for lce_workspace_size */
+#define LCE_OP_FORWARD 0
+#define LCE_OP_BACKWARD 1
+#define LCE_OP_FWD_BWD 2
+
+/* device status bits returned by lce_read_device_status */
+#define LCE_DEVICE_LABEL_RANGE 1
+#define LCE_DEVICE_TIMEOUT 2
+
+typedef struct lce_opts {
+  int64_t chunk_tokens;     /* tokens per chunk; 0 = automatic (4096, capped at N) */
+  int64_t ignore_index;     /* label value that is ignored; default -100 */
+  int64_t n_valid_override; /* < 0: count valid labels of this call; >= 0: use as the
+                               denominator n (data-parallel shards pass the global count) */
+  int32_t reduction;        /* LCE_MEAN (default) or LCE_SUM */
+  int32_t accumulate_dW;    /* 0: dW = G^T H; 1: dW += G^T H (gradient accumulation) */
+  int32_t sync_check;       /* 1: synchronise the stream at the end and turn device
+                               status bits into the return code */
+  int32_t reserved;         /* must be 0 */
+} lce_opts;
+
+/* Fill *opts with the defaults above. */
+void lce_opts_init(lce_opts* opts);
+
+/* Bytes of device workspace one call of the given op needs (LCE_OP_*). opts
+ * may be NULL (defaults). Returns 0 for invalid sizes. */
+size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opts* opts);
+
+/* Forward: loss [1] and lse [N] (fp32, device). lse of ignored rows is
+ * computed too (the backward needs it for nothing, callers may use it).
+ * N = 0 gives loss = 0. */
+int lce_forward(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                float* loss, float* lse, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward from a saved lse [N] (device, from lce_forward of the same inputs)
+ * and the upstream gradient grad_loss [1] (device fp32; NULL means 1.0).
+ * Recomputes the logits chunk by chunk. Writes dH [N, d] (bf16) and dW [V, d]
+ * (fp32; overwritten, or accumulated into when opts->accumulate_dW). */
+int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                 const float* lse, const float* grad_loss, void* dH, float* dW, const lce_opts* opts,
+                 void* ws, size_t ws_bytes, void* stream);
+
+/* Forward and backward in one call (the training step's loss head).
+ * grad_loss: device fp32 [1] or NULL for 1.0. lse may be NULL (kept in the
+ * workspace). Outputs as in lce_forward and lce_backward. */
+int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts,
+                void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise the stream and copy the workspace's device status bits
+ * (LCE_DEVICE_*) of the last call that used ws into *flags. */
+int lce_read_device_status(const void* ws, void* stream, int* flags);
+
+/* Static, human-readable text for a status code. */
+const char* lce_status_string(int status);
+
+/* LCE_VERSION of the built library. */
+int lce_version(void);
+
+/*
+ * Measurement hook (for benchmarks; off by default). Between
+ * lce_profile_begin() and lce_profile_end(), every kernel the library
+ * launches is bracketed by two CUDA events recorded on the launch stream, so
+ * each kernel's device time is measured where it runs, inside the caller's
+ * step. lce_profile_end() synchronises those events and returns, per kernel
+ * kind, the number of launches, their summed device time and their summed
+ * algorithmic work (bytes for memory-bound kinds, flops for the GEMMs).
+ * Events come from a pool the library owns (created on first use, no device
+ * memory is allocated). Not thread-safe: one profiling thread at a time.
+ */
+#define LCE_KERNEL_KINDS 8
+typedef struct lce_profile {
+  int32_t launches[LCE_KERNEL_KINDS];
+  double ms[LCE_KERNEL_KINDS];      /* summed device time per kind */
+  double work[LCE_KERNEL_KINDS];    /* summed algorithmic flops (GEMMs) or bytes (others) */
+} lce_profile;
+
+int lce_profile_begin(void);
+int lce_profile_end(lce_profile* out);
+/* Name of a kernel kind (0 .. LCE_KERNEL_KINDS-1), or NULL. */
+const char* lce_kernel_name(int kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LCE_H_ */

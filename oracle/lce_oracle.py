@@ -221,17 +221,15 @@ def dH_rows_f64(H, W, y, rows, scale, *, ignore_index=IGNORE_INDEX):
     rows = np.asarray(rows, dtype=np.int64)
     y = np.asarray(y, dtype=np.int64)
     W64 = np.asarray(W, dtype=np.float64)
-    out = np.zeros((rows.size, W64.shape[1]))
-    for j, i in enumerate(rows):
-        if y[i] == ignore_index:
-            continue
-        z = np.asarray(H[i], dtype=np.float64) @ W64.T
-        m = z.max()
-        lse = m + math.log(np.exp(z - m).sum())
-        p = np.exp(z - lse)
-        p[y[i]] -= 1.0
-        out[j] = (p * scale) @ W64
-    return out
+    yr = y[rows]
+    valid = yr != ignore_index
+    z = np.asarray(H[rows], dtype=np.float64) @ W64.T          # logits of the sampled rows
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    p = np.exp(z - lse[:, None])
+    p[np.nonzero(valid)[0], yr[valid]] -= 1.0
+    G = p * (valid * scale)[:, None]
+    return G @ W64
 
 
 def dW_rows_f64(H, W, y, lse, vrows, scale, *, ignore_index=IGNORE_INDEX):

@@ -1,0 +1,136 @@
+"""The C-ABI library: it builds, loads, exports every symbol include/lce.h
+declares, and rejects bad arguments on the host before touching a device.
+CPU only (no compute calls)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from chunked_lm_head_linear_gb300 import build, lce
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lce.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return lce.load()
+
+
+def _declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(lce_[a-z_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert _declared_functions() == sorted(lce.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {lce.LIB_PATH}").read()
+    for name in _declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_version_and_status_strings(lib):
+    assert lib.lce_version() == 1
+    for code in range(8):
+        s = lce.status_string(code)
+        assert s and s != "unknown status"
+    assert lce.status_string(99) == "unknown status"
+
+
+def test_opts_defaults(lib):
+    o = lce.LceOpts()
+    lib.lce_opts_init(ctypes.byref(o))
+    assert (o.chunk_tokens, o.ignore_index, o.n_valid_override, o.reduction,
+            o.accumulate_dW, o.sync_check, o.reserved) == (0, -100, -1, 0, 0, 0, 0)
+    assert ctypes.sizeof(lce.LceOpts) == 40
+
+
+def test_workspace_size(lib):
+    V, d = 151936, 2048
+    fwd = lce.workspace_size(lce.LCE_OP_FORWARD, 8192, d, V)
+    bwd = lce.workspace_size(lce.LCE_OP_BACKWARD, 8192, d, V)
+    both = lce.workspace_size(lce.LCE_OP_FWD_BWD, 8192, d, V)
+    assert 0 < fwd < bwd < both
+    # extra memory grows with the chunk, not with N
+    o = lce.make_opts(chunk_tokens=1024)
+    a = lce.workspace_size(lce.LCE_OP_FWD_BWD, 65536, 4096, V, o)
+    b = lce.workspace_size(lce.LCE_OP_FWD_BWD, 8 * 65536, 4096, V, o)
+    assert b - a < 8 * 65536 * 16          # only per-token vectors scale with N
+    assert a < 65536 * V * 4 / 8           # far below the unfused fp32 logits
+    assert lce.workspace_size(lce.LCE_OP_FWD_BWD, 8192, 7, V) == 0      # d % 8 != 0
+    assert lce.workspace_size(lce.LCE_OP_FWD_BWD, -1, 8, V) == 0
+    assert lce.workspace_size(7, 8, 8, 8) == 0
+
+
+FAKE = 0x100000  # an aligned non-null address; never dereferenced by host-side checks
+
+
+def _call_fwd(lib, H=FAKE, W=FAKE, y=FAKE, N=256, d=256, V=4096, loss=FAKE, lse=FAKE, opts=None,
+              ws=FAKE, ws_bytes=1 << 40):
+    o = opts if opts is not None else lce.make_opts()
+    return lib.lce_forward(H, W, y, N, d, V, loss, lse, ctypes.byref(o), ws, ws_bytes, None)
+
+
+def test_host_side_argument_errors(lib):
+    E = lce
+    assert _call_fwd(lib, W=None) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, H=None) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, y=None) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, d=12) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, d=0) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, V=0) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, N=-5) == E.LCE_ERR_INVALID_ARG
+    assert _call_fwd(lib, H=FAKE + 8) == E.LCE_ERR_ALIGNMENT
+    assert _call_fwd(lib, ws=FAKE + 64) == E.LCE_ERR_ALIGNMENT
+    assert _call_fwd(lib, ws_bytes=16) == E.LCE_ERR_WORKSPACE
+    bad = lce.make_opts()
+    bad.reduction = 7
+    assert _call_fwd(lib, opts=bad) == E.LCE_ERR_INVALID_ARG
+    bad = lce.make_opts()
+    bad.reserved = 1
+    assert _call_fwd(lib, opts=bad) == E.LCE_ERR_INVALID_ARG
+    o = lce.make_opts()
+    P = FAKE
+    assert lib.lce_backward(P, P, P, 16, 8, 8, None, None, P, P, ctypes.byref(o), P, 1 << 30, None) \
+        == E.LCE_ERR_INVALID_ARG                      # lse missing
+    assert lib.lce_fwd_bwd(P, P, P, 16, 8, 8, None, P, None, None, P, ctypes.byref(o), P, 1 << 30, None) \
+        == E.LCE_ERR_INVALID_ARG                      # dH missing
+    flags = ctypes.c_int()
+    assert lib.lce_read_device_status(None, None, ctypes.byref(flags)) == E.LCE_ERR_INVALID_ARG
+
+
+def test_valid_call_without_a_gpu_fails_cleanly(lib):
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    rc = _call_fwd(lib)
+    assert rc in (lce.LCE_ERR_CUDA, lce.LCE_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_binding_refuses_cpu_tensors():
+    torch = pytest.importorskip("torch")
+    H = torch.zeros(4, 8, dtype=torch.bfloat16)
+    W = torch.zeros(3, 8, dtype=torch.bfloat16)
+    y = torch.zeros(4, dtype=torch.int64)
+    with pytest.raises(ValueError):
+        lce.lce_forward(H, W, y)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import importlib
+    mod = importlib.import_module("chunked_lm_head_linear_gb300.lce")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        saved = mod._lib
+        mod._lib = None
+        try:
+            mod.load(str(tmp_path / "missing.so"))
+        finally:
+            mod._lib = saved

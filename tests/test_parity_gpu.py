@@ -1,0 +1,304 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
+
+Tolerances (written here, derived in the design doc):
+  loss: relative error <= 1e-3;  dH, dW: relative Frobenius error <= 5e-3;
+  lse: max relative error <= 1e-4 (fp32 logits and sum-exp; the fp64 oracle
+  differs only by fp32 accumulation and exp rounding, ~1e-6);
+  the softmax-only rows of dW (vocabulary rows no valid label hits) are also
+  held to 5e-3 on their own, because in the full dW the one-hot rows dominate
+  the norm and would hide an error in the softmax part.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from chunked_lm_head_linear_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_LOSS = 1e-3
+TOL_GRAD = 5e-3
+TOL_LSE = 1e-4
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def to_dev(inp):
+    torch = _torch()
+    H = torch.from_numpy(np.ascontiguousarray(inp["H"]).view(np.int16)).view(torch.bfloat16).cuda()
+    W = torch.from_numpy(np.ascontiguousarray(inp["W"]).view(np.int16)).view(torch.bfloat16).cuda()
+    y = torch.from_numpy(np.ascontiguousarray(inp["y"])).cuda()
+    return H, W, y
+
+
+def rel_fro(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = np.linalg.norm(b)
+    return float(np.linalg.norm(a - b) / (den if den > 0 else 1.0))
+
+
+def bf16_to_np(t):
+    torch = _torch()
+    return t.float().cpu().numpy().astype(np.float64) if t.dtype == torch.bfloat16 else t.cpu().numpy()
+
+
+def small_inputs(N, d, V, seed=0, ignore_frac=0.1, sigma_w=0.02, labels="uniform"):
+    w = inputs.Workload(f"n{N}_d{d}_v{V}", N=N, d=d, V=V, sigma_w=sigma_w, labels=labels,
+                        ignore="random" if ignore_frac > 0 else "none", ignore_frac=ignore_frac, seed=seed)
+    return inputs.make_inputs(w)
+
+
+def check_against_oracle(ref, y, loss, lse, dH=None, dW=None, V=None):
+    assert abs(float(loss) - ref["loss"]) <= TOL_LOSS * max(abs(ref["loss"]), 1e-30) + 1e-7
+    lse = np.asarray(lse, dtype=np.float64)
+    assert np.max(np.abs(lse - ref["lse"]) / np.maximum(np.abs(ref["lse"]), 1.0)) <= TOL_LSE
+    if dH is not None:
+        assert rel_fro(dH, ref["dH"]) <= TOL_GRAD
+    if dW is not None:
+        assert rel_fro(dW, ref["dW"]) <= TOL_GRAD
+        hit = np.zeros(ref["dW"].shape[0], dtype=bool)
+        hit[y[y != oracle.IGNORE_INDEX]] = True
+        if (~hit).any() and np.linalg.norm(ref["dW"][~hit]) > 0:
+            assert rel_fro(dW[~hit], ref["dW"][~hit]) <= TOL_GRAD
+
+
+# ---------------------------------------------------------------------------
+# Small cases: full oracle, element by element
+# ---------------------------------------------------------------------------
+
+def test_tiny_workload_fwd_bwd(cuda_lib):
+    inp = inputs.make_inputs("tiny_n256_d256_v4096")
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+def test_tiny_workload_split_forward_backward(cuda_lib):
+    torch = _torch()
+    inp = inputs.make_inputs("tiny_n256_d256_v4096")
+    g = 0.37
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"], grad_loss=g)
+    H, W, y = to_dev(inp)
+    loss, lse = cuda_lib.lce_forward(H, W, y, sync_check=True)
+    gl = torch.tensor([g], dtype=torch.float32, device="cuda")
+    dH, dW = cuda_lib.lce_backward(H, W, y, lse, gl, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+RAGGED = [
+    # N, d, V, chunk      what it exercises
+    (300, 136, 1000, 128),   # row tail, K tail (136 = 2*64 + 8), partial d tile, vocab tail
+    (129, 72, 517, 64),      # one row past a tile, chunks smaller than a tile
+    (513, 264, 4099, 200),   # chunk not a multiple of the tile, 3-column vocab tail
+    (1, 64, 300, 0),         # a single token
+    (40, 8, 2, 0),           # two classes, d = 8 (smallest legal hidden size)
+    (200, 512, 257, 0),      # vocabulary one past a tile
+]
+
+
+@pytest.mark.parametrize("N,d,V,chunk", RAGGED)
+def test_ragged_shapes(cuda_lib, N, d, V, chunk):
+    inp = small_inputs(N, d, V, seed=N + d + V, sigma_w=0.05)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=chunk, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+def test_large_logits_and_zipf_labels(cuda_lib):
+    """Logit spread of tens of nats (sigma_w = 1): exercises the max subtraction."""
+    inp = small_inputs(384, 128, 3000, seed=5, sigma_w=1.0, labels="zipf")
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+def test_reduction_sum_grad_scale_and_override(cuda_lib):
+    torch = _torch()
+    inp = small_inputs(300, 128, 1500, seed=9)
+    H, W, y = to_dev(inp)
+    gl = torch.tensor([2.5], dtype=torch.float32, device="cuda")
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"], reduction=oracle.SUM, grad_loss=2.5)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, gl, reduction="sum", sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"], n_valid_override=1000, grad_loss=2.5)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, gl, n_valid_override=1000, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+def test_accumulate_dW(cuda_lib):
+    torch = _torch()
+    inp = small_inputs(256, 64, 700, seed=11)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    base = torch.randn(700, 64, device="cuda", dtype=torch.float32)
+    dW = base.clone()
+    cuda_lib.lce_fwd_bwd(H, W, y, dW=dW, accumulate_dW=True, chunk_tokens=96, sync_check=True)
+    assert rel_fro((dW - base).cpu().numpy(), ref["dW"]) <= TOL_GRAD
+
+
+def test_all_ignored_and_empty(cuda_lib):
+    torch = _torch()
+    inp = small_inputs(130, 64, 600, seed=3)
+    inp["y"][:] = oracle.IGNORE_INDEX
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, sync_check=True)
+    assert loss.item() == 0.0
+    assert torch.count_nonzero(dH).item() == 0 and torch.count_nonzero(dW).item() == 0
+    np.testing.assert_allclose(lse.cpu().numpy(), ref["lse"], rtol=TOL_LSE)
+    # N = 0
+    H0 = H[:0]
+    y0 = y[:0]
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H0, W, y0, sync_check=True)
+    assert loss.item() == 0.0 and lse.numel() == 0 and torch.count_nonzero(dW).item() == 0
+
+
+def test_label_out_of_range_is_reported_and_ignored(cuda_lib):
+    inp = small_inputs(200, 64, 500, seed=4)
+    y_bad = inp["y"].copy()
+    y_bad[[7, 150]] = [500, -3]
+    H, W, _ = to_dev(inp)
+    torch = _torch()
+    y = torch.from_numpy(y_bad).cuda()
+    with pytest.raises(cuda_lib.LCEError) as e:
+        cuda_lib.lce_fwd_bwd(H, W, y, sync_check=True)
+    assert e.value.code == cuda_lib.LCE_ERR_LABEL_RANGE
+    # without sync_check the call returns OK, the status bit is set, and the
+    # bad rows count as ignored
+    ws = torch.empty(cuda_lib.workspace_size(cuda_lib.LCE_OP_FWD_BWD, 200, 64, 500), dtype=torch.uint8,
+                     device="cuda")
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, workspace=ws)
+    assert cuda_lib.read_device_status(ws) & cuda_lib.LCE_DEVICE_LABEL_RANGE
+    y_ign = y_bad.copy()
+    y_ign[[7, 150]] = oracle.IGNORE_INDEX
+    ref = oracle.lce_bf16(inp["H"], inp["W"], y_ign)
+    check_against_oracle(ref, y_ign, loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
+def test_chunk_size_invariance_and_determinism(cuda_lib):
+    """loss, lse and dH are row-local with a fixed vocabulary order: bitwise
+    equal for every chunk size; dW differs only by fp32 reassociation."""
+    torch = _torch()
+    inp = small_inputs(700, 256, 4096, seed=21)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    outs = {}
+    for C in (64, 128, 256, 700, 1000):
+        outs[C] = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=C, sync_check=True)
+    base = outs[128]
+    for C, o in outs.items():
+        assert torch.equal(o[0], base[0]), C
+        assert torch.equal(o[1], base[1]), C
+        assert torch.equal(o[2], base[2]), C
+        assert rel_fro(o[3].cpu().numpy(), base[3].cpu().numpy()) <= 1e-6, C
+        check_against_oracle(ref, inp["y"], o[0].item(), o[1].cpu().numpy(), bf16_to_np(o[2]), o[3].cpu().numpy())
+    again = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=128, sync_check=True)
+    for a, b in zip(again, base):
+        assert torch.equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads: sampled rows against the oracle, properties on all of it
+# ---------------------------------------------------------------------------
+
+def _stratified_rows(y, N, rng, k=128):
+    ign = np.nonzero(y == oracle.IGNORE_INDEX)[0]
+    frequent = np.nonzero(y == 0)[0]
+    picks = [np.arange(min(8, N)), np.arange(max(0, N - 8), N), ign[:8], frequent[:8],
+             rng.choice(N, size=k, replace=False)]
+    return np.unique(np.concatenate(picks))[:k + 40]
+
+
+def _stratified_vocab(V, y, rng, k=128):
+    labels, counts = np.unique(y[y != oracle.IGNORE_INDEX], return_counts=True)
+    top = labels[np.argsort(-counts)[:8]]
+    tail_tile = np.arange(max(0, V - 64), V)
+    picks = [np.arange(10), top, tail_tile[:: max(1, tail_tile.size // 16)], [V - 1],
+             rng.choice(V, size=k, replace=False)]
+    return np.unique(np.concatenate(picks))
+
+
+def sampled_full_check(cuda_lib, name, chunk_tokens=0):
+    torch = _torch()
+    gpath = os.path.join(GOLDEN, f"full_{name}.npz")
+    if not os.path.exists(gpath):
+        pytest.fail(f"missing cached oracle values {gpath} (tests/golden/make_full_golden.py writes them)")
+    gold = np.load(gpath)
+    inp = inputs.make_inputs(name)
+    if str(gold["digest"]) != inputs.input_digest(inp):
+        pytest.fail("input generator output differs from the one the cached oracle values were made for")
+    w = inp["workload"]
+    y_np = inp["y"]
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=chunk_tokens, sync_check=True)
+    torch.cuda.synchronize()
+    # loss and every lse against the oracle
+    assert abs(loss.item() - float(gold["loss"])) <= TOL_LOSS * abs(float(gold["loss"]))
+    lse_np = lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse_np - gold["lse"]) / np.maximum(np.abs(gold["lse"]), 1.0)) <= TOL_LSE
+    # sampled rows of dH and vocabulary rows of dW
+    rng = np.random.default_rng(123)
+    Hf = inputs.bf16_bits_to_f32(inp["H"])
+    Wf = inputs.bf16_bits_to_f32(inp["W"])
+    scale, _ = oracle.grad_scale(y_np)
+    R = _stratified_rows(y_np, w.N, rng)
+    dH_ref = oracle.dH_rows_f64(Hf, Wf, y_np, R, scale)
+    dH_gpu = dH[torch.from_numpy(R).cuda()].float().cpu().numpy()
+    assert rel_fro(dH_gpu, dH_ref) <= TOL_GRAD
+    S = _stratified_vocab(w.V, y_np, rng)
+    dW_ref = oracle.dW_rows_f64(Hf, Wf, y_np, gold["lse"], S, scale)
+    dW_gpu = dW[torch.from_numpy(S).cuda()].cpu().numpy()
+    assert rel_fro(dW_gpu, dW_ref) <= TOL_GRAD
+    hit = np.isin(S, y_np[y_np != oracle.IGNORE_INDEX])
+    if (~hit).sum() > 4:
+        assert rel_fro(dW_gpu[~hit], dW_ref[~hit]) <= TOL_GRAD
+    # properties on the whole outputs: sum_v dW_v = 0 and <dH, H> = <dW, W>
+    colsum = dW.double().sum(dim=0)
+    assert (colsum.norm() / dW.double().norm()).item() <= TOL_GRAD
+    a = (dH.double() * H.double()).sum().item()
+    b = (dW.double() * W.double()).sum().item()
+    assert abs(a - b) <= TOL_GRAD * max(abs(a), abs(b))
+    return loss, lse, dH, dW
+
+
+def test_full_qwen2b_workload(cuda_lib):
+    sampled_full_check(cuda_lib, "qwen2b_n8192_d2048_v151936")
+
+
+@pytest.mark.slow
+def test_full_packed_workload(cuda_lib):
+    sampled_full_check(cuda_lib, "packed_n32768_d2048_v151936")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["moe_n16384_d7168_v129280", "moe_n16384_d7168_v151655"])
+def test_full_moe_workloads(cuda_lib, name):
+    sampled_full_check(cuda_lib, name)
+
+
+@pytest.mark.slow
+def test_full_seq64k_chunk_sweep(cuda_lib):
+    """64k-token head, chunk sizes 1024..8192: every chunk size within the oracle
+    tolerance; lse and dH bitwise equal across chunk sizes; dW within 1e-6."""
+    torch = _torch()
+    name = "seq64k_n65536_d4096_v151936"
+    first = None
+    for C in (1024, 2048, 4096, 8192):
+        loss, lse, dH, dW = sampled_full_check(cuda_lib, name, chunk_tokens=C)
+        if first is None:
+            first = (loss.clone(), lse.clone(), dH.clone(), dW.clone())
+        else:
+            assert torch.equal(loss, first[0]) and torch.equal(lse, first[1]) and torch.equal(dH, first[2])
+            assert ((dW - first[3]).norm() / first[3].norm()).item() <= 1e-6
+        del loss, lse, dH, dW
+        torch.cuda.empty_cache()
