@@ -129,22 +129,22 @@ def gpu_uuid(torch):
 # ---------------------------------------------------------------------------
 # CPU oracle timing (reported baseline)
 # ---------------------------------------------------------------------------
-def oracle_sample_time(inp, rows: int):
-    """Time the fp64 oracle (fwd + bwd, full V and d) on the first ``rows`` tokens."""
+def cpu_baseline(inp, target_s=12.0, max_rows=4096):
+    """Time the fp64 oracle (forward + backward at full d and V) on the first
+    rows of the workload, sized to about ``target_s`` seconds of CPU work."""
     import oracle
-    H = oracle.decode_bf16(inp["H"][:rows])
-    W = oracle.decode_bf16(inp["W"])
-    y = inp["y"][:rows]
-    t0 = time.perf_counter()
-    oracle.lce_f64(H, W, y)
-    return time.perf_counter() - t0
+    Wd = oracle.decode_bf16(inp["W"])
 
+    def run(rows):
+        Hd = oracle.decode_bf16(inp["H"][:rows])
+        t0 = time.perf_counter()
+        oracle.lce_f64(Hd, Wd, inp["y"][:rows])
+        return time.perf_counter() - t0
 
-def cpu_baseline(inp, target_s=12.0, max_rows=2048):
-    t16 = oracle_sample_time(inp, 16)
-    rows = int(min(max_rows, max(16, 16 * target_s / max(t16, 1e-3))))
-    rows = max(16, rows // 16 * 16)
-    t = oracle_sample_time(inp, rows)
+    t32 = run(32)
+    rows = int(min(max_rows, inp["H"].shape[0], max(32, 32 * target_s / max(t32, 1e-3))))
+    rows = max(32, rows // 32 * 32)
+    t = run(rows)
     return {"value": rows / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"first {rows} tokens of the workload at full d and V, numpy fp64 oracle "
                       f"(forward + backward), {t:.1f} s; BLAS threads = all host cores"}
@@ -196,11 +196,13 @@ def config_of(w, chunk, args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=inputs.BENCH_WORKLOAD, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--chunk", type=int, default=4096)
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the workload's token count (same d, V and label law); for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
@@ -209,13 +211,15 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     w = inputs.WORKLOADS[args.workload]
+    if args.tokens > 0:
+        w = w.scaled(N=args.tokens, name=f"{w.name}_tokens{args.tokens}")
     if args.impl == "reference":
         run_reference(args, w)
         return
 
     import torch
     import torch.distributed as dist
-    from chunked_lm_head_linear_gb300 import lce
+    from chunked_lm_head_linear_gb300 import dp, lce
 
     torch.cuda.set_device(local)
     if world > 1:
@@ -231,15 +235,10 @@ def main():
     W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
     H = H_host.to(dev)
     y = y_host.to(dev)
-    n_local = int((inp["y"] != inputs.IGNORE_INDEX).sum())
-    n_global = n_local
-    if world > 1:
-        t = torch.tensor([n_local], dtype=torch.int64, device=dev)
-        dist.all_reduce(t)
-        n_global = int(t.item())
+    n_global = dp.global_valid_count(y) if world > 1 else -1
 
     chunk = min(args.chunk, N) if args.chunk > 0 else 0
-    opts = dict(chunk_tokens=chunk, n_valid_override=n_global if world > 1 else -1)
+    opts = dict(chunk_tokens=chunk, n_valid_override=n_global)
     ws = torch.empty(lce.workspace_size(lce.LCE_OP_FWD_BWD, N, d, V, lce.make_opts(**opts)), dtype=torch.uint8,
                      device=dev)
     dW = torch.empty((V, d), dtype=torch.float32, device=dev)
@@ -247,10 +246,11 @@ def main():
     stream = torch.cuda.current_stream()
 
     def step(Hx, yx):
-        loss, _, dH, _ = lce.lce_fwd_bwd(Hx, W, yx, dW=dW, lse=lse, workspace=ws, **opts)
         if world > 1:
-            dist.all_reduce(dW)
-            dist.all_reduce(loss)
+            loss, _, dH, _ = dp.dp_fwd_bwd(Hx, W, yx, n_global=n_global, dW=dW, lse=lse, workspace=ws,
+                                           chunk_tokens=chunk)
+        else:
+            loss, _, dH, _ = lce.lce_fwd_bwd(Hx, W, yx, dW=dW, lse=lse, workspace=ws, **opts)
         return loss, dH
 
     def barrier():
