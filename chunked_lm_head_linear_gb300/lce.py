@@ -35,7 +35,7 @@ LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
 # Every symbol include/lce.h declares.
 EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
-            "lce_profile_end", "lce_kernel_name")
+            "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc")
 LCE_KERNEL_KINDS = 8
 
 
@@ -94,6 +94,8 @@ def load(path: str | None = None):
         lib.lce_profile_begin.restype = I32
         lib.lce_profile_end.argtypes = [ctypes.POINTER(LceProfile)]
         lib.lce_profile_end.restype = I32
+        lib.lce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P]
+        lib.lce_forward_noalloc.restype = I32
         lib.lce_kernel_name.argtypes = [I32]
         lib.lce_kernel_name.restype = ctypes.c_char_p
         _lib = lib

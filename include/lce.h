@@ -114,6 +114,24 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
                 const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* Forward that allocates nothing and takes no workspace, for callers that
+ * cannot allocate device memory: their memory is wholly owned by another
+ * allocator (a framework's caching pool or a runtime's arena), or they must
+ * not call cudaMalloc / cudaFree, which can block or synchronise the device.
+ * The pages have no counterpart to this entry point; it is a deployment aid.
+ * Same arguments and results as lce_forward, minus ws / ws_bytes. Its scratch
+ * is a fixed 32 MiB array inside the library's device image, held on every
+ * GPU that loads the library until the process exits; a call whose forward
+ * workspace (lce_workspace_size(LCE_OP_FORWARD, ...)) exceeds 32 MiB returns
+ * LCE_ERR_WORKSPACE (pass a smaller opts->chunk_tokens). The first call on a
+ * device looks up the array's device address (make it before any stream
+ * capture). All calls share the one array: calls whose work overlaps on the
+ * GPU (other streams, other host threads) race and must be serialised by the
+ * caller. Nothing in the array needs to be zero on entry; each call
+ * overwrites what it reads, and lce_read_device_status() does not apply. */
+int lce_forward_noalloc(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                        float* loss, float* lse, const lce_opts* opts, void* stream);
+
 /* Synchronise the stream and copy the workspace's device status bits
  * (LCE_DEVICE_*) of the last call that used ws into *flags. */
 int lce_read_device_status(const void* ws, void* stream, int* flags);
