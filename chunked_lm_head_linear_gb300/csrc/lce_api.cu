@@ -4,17 +4,22 @@
 // launch goes to the caller's stream and nothing synchronises the host unless
 // the caller asks for it (opts->sync_check).
 //
-// Launch sequence per call ("XTuner on Ascend 910C: Qwen3.5-2B training
+// Launch sequence of lce_fwd_bwd ("XTuner on Ascend 910C: Qwen3.5-2B training
 // optimisation", section 3.1.4; tokens in chunks as in "XTuner V1
 // introduction", memory optimisation section):
 //   prepare                      label scan -> n, g/n, range-error bit
 //   for each chunk of C tokens:
-//     logits GEMM (FWD_STATS)    z tiles -> per-tile (max, sum-exp), z_{i,y_i}
-//     combine                    lse_i, loss_i
-//     logits GEMM (FWD_GRAD)     gradient tile G (bf16, [C, V]) from lse     (backward)
-//     dH GEMM                    dH_c = G_c W                                (backward)
-//     dW GEMM                    dW (+)= G_c^T H_c                           (backward)
+//     logits GEMM (FWD_REF)      row reference: max over the first vocabulary tile
+//     logits GEMM (FWD_STATS_P)  per-tile (max, sum-exp), z_{i,y_i}, exp tile P
+//     combine                    lse_i, loss_i, alpha_i = exp(ref_i - lse_i), label entry of P
+//     logits GEMM (FWD_GRAD)     only if a logit exceeded its reference by > 60 nats:
+//                                the exact gradient tile replaces P (alpha = 1)
+//     hscale                     Ht = alpha * H_c
+//     dH GEMM                    dH_c = (g/n) alpha (P W)
+//     dW GEMM                    dW (+)= (g/n) P^T Ht
 //   finalize                     loss = sum_i loss_i / n
+// lce_forward runs prepare, FWD_STATS + combine per chunk, finalize;
+// lce_backward recomputes: FWD_GRAD (from the saved lse), dH and dW GEMMs.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -56,10 +61,12 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-  int64_t C = 0;     // tokens per chunk
-  int64_t T = 0;     // vocabulary tiles per row
-  int64_t ldp = 0;   // row stride (elements) of the gradient tile buffer
-  size_t status = 0, loss_i = 0, lse = 0, ztgt = 0, partials = 0, P = 0, total = 0;
+  int64_t C = 0;       // tokens per chunk
+  int64_t T = 0;       // vocabulary tiles per row
+  int64_t ldp = 0;     // row stride (elements) of the exp / gradient tile buffer
+  int64_t chunks = 0;  // number of chunks
+  size_t status = 0, loss_i = 0, lse = 0, ztgt = 0, partials = 0, P = 0;
+  size_t ref = 0, alpha = 0, guard = 0, Ht = 0, total = 0;
 };
 
 int64_t chunk_of(int64_t N, const lce_opts* o) {
@@ -70,7 +77,6 @@ int64_t chunk_of(int64_t N, const lce_opts* o) {
 }
 
 Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
-  (void)d;
   Layout L;
   L.C = chunk_of(N, o);
   L.T = ceil_div(V, kVocabTile);
@@ -89,7 +95,14 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
     L.ztgt = take(sizeof(float) * static_cast<size_t>(L.C));
     L.partials = take(sizeof(float) * 2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.T));
   }
-  if (op == LCE_OP_FWD_BWD) L.lse = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+  L.chunks = N > 0 ? ceil_div(N, L.C) : 0;
+  if (op == LCE_OP_FWD_BWD) {
+    L.lse = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+    L.ref = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.alpha = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.guard = take(sizeof(int) * static_cast<size_t>(L.chunks > 0 ? L.chunks : 1));
+    L.Ht = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(d));
+  }
   if (bwd) L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
   L.total = off;
   return L;
@@ -155,16 +168,19 @@ int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64
 // ---------------------------------------------------------------------------
 enum Kind : int {
   K_PREPARE = 0,
-  K_LOGITS_STATS = 1,
+  K_LOGITS_STATS = 1,   // FWD_STATS and FWD_STATS_P
   K_COMBINE = 2,
-  K_LOGITS_GRAD = 3,
+  K_LOGITS_GRAD = 3,    // unconditional FWD_GRAD (lce_backward)
   K_GEMM_DH = 4,
   K_GEMM_DW = 5,
   K_FINALIZE = 6,
-  K_OTHER = 7,
+  K_OTHER = 7,          // memsets and the guard-conditional FWD_GRAD (work counted as 0)
+  K_LOGITS_REF = 8,
+  K_HSCALE = 9,
 };
-const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare", "logits_stats", "combine", "logits_grad",
-                                                  "gemm_dH", "gemm_dW", "finalize", "other"};
+const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",  "logits_stats", "combine",    "logits_grad",
+                                                  "gemm_dH",  "gemm_dW",      "finalize",   "other",
+                                                  "logits_ref", "hscale"};
 
 struct ProfRecord {
   int kind;
@@ -221,15 +237,25 @@ struct Call {
 };
 
 // Logits GEMM for one chunk, in one of the FwdMode epilogues.
-int logits_gemm(const Call& c, int64_t c0, int64_t rows, int mode, float* lse_rows, uint16_t* P) {
+struct LogitsArgs {
+  int mode = lce::FWD_STATS;
+  const float* lse_rows = nullptr;  // FWD_GRAD
+  uint16_t* P = nullptr;            // FWD_STATS_P, FWD_GRAD
+  float* ref = nullptr;             // FWD_REF out, FWD_STATS_P in
+  int* guard = nullptr;             // FWD_STATS_P
+  const int* only_if = nullptr;     // conditional launch
+};
+
+int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   CUtensorMap mA, mB;
   LCE_TRY(make_map(&mA, c.H + c0 * c.d, rows, c.d, c.d, lce::kTileM));
   LCE_TRY(make_map(&mB, c.W, c.V, c.d, c.d, lce::kTileN));
-  lce::GemmGeomHost g{static_cast<int>(ceil_div(rows, lce::kTileM)), static_cast<int>(c.L.T),
+  const int n_tiles = a.mode == lce::FWD_REF ? 1 : static_cast<int>(c.L.T);
+  lce::GemmGeomHost g{static_cast<int>(ceil_div(rows, lce::kTileM)), n_tiles,
                       static_cast<int>(ceil_div(c.d, lce::kTileK)), 1};
   lce::FwdParams p;
   std::memset(&p, 0, sizeof p);
-  p.mode = mode;
+  p.mode = a.mode;
   p.rows = static_cast<int>(rows);
   p.V = static_cast<int>(c.V);
   p.ntiles_v = static_cast<int>(c.L.T);
@@ -237,17 +263,26 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, int mode, float* lse_ro
   p.y = c.y + c0;
   p.partials = reinterpret_cast<float2*>(c.ws + c.L.partials);
   p.ztgt = reinterpret_cast<float*>(c.ws + c.L.ztgt);
-  p.lse = lse_rows;
-  p.P = reinterpret_cast<__nv_bfloat16*>(P);
+  p.ref = a.ref;
+  p.lse = a.lse_rows;
+  p.P = reinterpret_cast<__nv_bfloat16*>(a.P);
   p.ldp = c.L.ldp;
   p.flags = &c.st->flags;
-  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
-  return timed(c.s, mode == lce::FWD_GRAD ? K_LOGITS_GRAD : K_LOGITS_STATS, flops,
+  p.guard = a.guard;
+  p.only_if = a.only_if;
+  const double flops =
+      2.0 * static_cast<double>(rows) * static_cast<double>(n_tiles == 1 ? lce::kTileN : c.V) * static_cast<double>(c.d);
+  int kind = K_LOGITS_STATS;
+  if (a.mode == lce::FWD_REF) kind = K_LOGITS_REF;
+  if (a.mode == lce::FWD_GRAD) kind = a.only_if ? K_OTHER : K_LOGITS_GRAD;
+  return timed(c.s, kind, a.only_if ? 0.0 : flops,
                [&] { return cuda_rc(lce::launch_fwd_gemm(mA, mB, g, p, c.dev.num_sms, c.s)); });
 }
 
 int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* loss_i) {
-  LCE_TRY(logits_gemm(c, c0, rows, lce::FWD_STATS, nullptr, nullptr));
+  LogitsArgs a;
+  a.mode = lce::FWD_STATS;
+  LCE_TRY(logits_gemm(c, c0, rows, a));
   const double bytes = static_cast<double>(rows) * (8.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4);
   return timed(c.s, K_COMBINE, bytes, [&] {
     return cuda_rc(lce::launch_combine(reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(c.L.T),
@@ -257,12 +292,14 @@ int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* lo
   });
 }
 
-int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, uint16_t* dH, float* dW,
-                   bool accumulate) {
-  uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
-  LCE_TRY(logits_gemm(c, c0, rows, lce::FWD_GRAD, const_cast<float*>(lse + c0), P));
+// dH_c = (g/n) [rowscale] (G W) and dW (+)= (g/n) G^T B, with G [rows, V] in
+// the chunk's tile buffer and B = H_c or Ht.
+int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, uint16_t* dH, float* dW,
+          bool accumulate) {
+  const uint16_t* P = reinterpret_cast<const uint16_t*>(c.ws + c.L.P);
+  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
 
-  // dH_c = G_c W : A = G_c [rows, V] K-major, B = W [V, d] read N-major.
+  // dH_c: A = G_c [rows, V] K-major, B = W [V, d] read N-major.
   CUtensorMap mG, mW;
   LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kTileM));
   LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, 64));
@@ -273,16 +310,15 @@ int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, ui
   dp.N = static_cast<int>(c.d);
   dp.out = reinterpret_cast<__nv_bfloat16*>(dH + c0 * c.d);
   dp.ld = c.d;
-  dp.rowscale = nullptr;
+  dp.rowscale = rowscale;
   dp.st = c.st;
-  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
   LCE_TRY(timed(c.s, K_GEMM_DH, flops,
                 [&] { return cuda_rc(lce::launch_dh_gemm(mG, mW, gh, dp, &c.st->flags, c.dev.num_sms, c.s)); }));
 
-  // dW (+)= G_c^T H_c : A = G_c^T (G_c read M-major), B = H_c [rows, d] read N-major.
-  CUtensorMap mGt, mH;
+  // dW: A = G_c^T (G_c read M-major), B = [rows, d] read N-major.
+  CUtensorMap mGt, mB;
   LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, 64));
-  LCE_TRY(make_map(&mH, c.H + c0 * c.d, rows, c.d, c.d, 64));
+  LCE_TRY(make_map(&mB, B, rows, c.d, c.d, 64));
   lce::GemmGeomHost gw{static_cast<int>(ceil_div(c.V, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
                        static_cast<int>(ceil_div(rows, lce::kTileK)), 0};
   lce::DwParams wp;
@@ -293,13 +329,72 @@ int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, ui
   wp.accumulate = accumulate ? 1 : 0;
   wp.st = c.st;
   return timed(c.s, K_GEMM_DW, flops,
-               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mH, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
+               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mB, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
+}
+
+// Backward of one chunk from a known lse: recompute the logits into the
+// exact gradient tile, then the two GEMMs.
+int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, uint16_t* dH, float* dW,
+                   bool accumulate) {
+  LogitsArgs a;
+  a.mode = lce::FWD_GRAD;
+  a.lse_rows = lse + c0;
+  a.P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
+  LCE_TRY(logits_gemm(c, c0, rows, a));
+  return dh_dw(c, c0, rows, nullptr, c.H + c0 * c.d, dH, dW, accumulate);
+}
+
+// Forward and backward of one chunk without recomputing the logits: the
+// forward stores the exp tile, the backward rescales it per row.
+int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* lse, float* loss_i, uint16_t* dH,
+                float* dW, bool accumulate) {
+  uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
+  float* ref = reinterpret_cast<float*>(c.ws + c.L.ref);
+  float* alpha = reinterpret_cast<float*>(c.ws + c.L.alpha);
+  int* guard = reinterpret_cast<int*>(c.ws + c.L.guard) + chunk;
+  uint16_t* Ht = reinterpret_cast<uint16_t*>(c.ws + c.L.Ht);
+
+  LogitsArgs a;
+  a.mode = lce::FWD_REF;
+  a.ref = ref;
+  LCE_TRY(logits_gemm(c, c0, rows, a));
+
+  a.mode = lce::FWD_STATS_P;
+  a.P = P;
+  a.guard = guard;
+  LCE_TRY(logits_gemm(c, c0, rows, a));
+
+  const double cbytes = static_cast<double>(rows) * (8.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2);
+  LCE_TRY(timed(c.s, K_COMBINE, cbytes, [&] {
+    return cuda_rc(lce::launch_combine_exp(reinterpret_cast<const float2*>(c.ws + c.L.partials),
+                                           static_cast<int>(c.L.T), static_cast<int>(rows),
+                                           reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0,
+                                           static_cast<int>(c.V), c.o.ignore_index, ref, guard, lse + c0, loss_i + c0,
+                                           alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp, c.s));
+  }));
+
+  LogitsArgs g;
+  g.mode = lce::FWD_GRAD;
+  g.lse_rows = lse + c0;
+  g.P = P;
+  g.only_if = guard;
+  LCE_TRY(logits_gemm(c, c0, rows, g));
+
+  const double hbytes = static_cast<double>(rows) * static_cast<double>(c.d) * 4.0 + 4.0 * static_cast<double>(rows);
+  LCE_TRY(timed(c.s, K_HSCALE, hbytes, [&] {
+    return cuda_rc(lce::launch_hscale(reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), alpha,
+                                      static_cast<int>(rows), static_cast<int>(c.d),
+                                      reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
+  }));
+  return dh_dw(c, c0, rows, alpha, Ht, dH, dW, accumulate);
 }
 
 int prepare(const Call& c, const float* grad_loss) {
+  int* guards = c.L.guard ? reinterpret_cast<int*>(c.ws + c.L.guard) : nullptr;
+  const int nguards = c.L.guard ? static_cast<int>(c.L.chunks) : 0;
   return timed(c.s, K_PREPARE, 8.0 * static_cast<double>(c.N), [&] {
     return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V), c.o.ignore_index, c.o.reduction,
-                                       c.o.n_valid_override, grad_loss, c.st, c.s));
+                                       c.o.n_valid_override, grad_loss, c.st, guards, nguards, c.s));
   });
 }
 
@@ -416,10 +511,10 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
   if (N == 0 && !c.o.accumulate_dW)
     LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
                   [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
-  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+  for (int64_t k = 0, c0 = 0; c0 < N; ++k, c0 += c.L.C) {
     const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
-    LCE_TRY(forward_chunk(c, c0, rows, lse_rows, loss_i));
-    LCE_TRY(backward_chunk(c, c0, rows, lse_rows, static_cast<uint16_t*>(dH), dW, c.o.accumulate_dW || c0 > 0));
+    LCE_TRY(fused_chunk(c, k, c0, rows, lse_rows, loss_i, static_cast<uint16_t*>(dH), dW,
+                        c.o.accumulate_dW || c0 > 0));
   }
   LCE_TRY(finalize(c, loss_i, loss));
   return finish(c);

@@ -75,6 +75,7 @@ template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmGeom g,
                 typename Epi::Params ep) {
+  if (Epi::skip(ep)) return;  // conditional launch whose condition is false: no work at all
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);

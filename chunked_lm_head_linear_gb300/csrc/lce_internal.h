@@ -27,9 +27,14 @@ struct DevStatus {
 
 enum FwdMode : int {
   FWD_STATS = 0,    // per-(row, vocab tile) max / sum-exp partials + target logit
+  FWD_STATS_P = 1,  // FWD_STATS + exp-tile P = bf16(exp(z - ref_row)) stored for the backward
   FWD_GRAD = 2,     // gradient tile exp(z - lse) - onehot (valid rows), from a known lse
   FWD_REF = 3,      // row maximum over the first vocabulary tile
 };
+
+// An exp-tile entry may exceed the row reference by at most this many nats;
+// beyond it the chunk falls back to the exact gradient tile (FWD_GRAD).
+constexpr float kRefGuardNats = 60.f;
 
 struct FwdParams {
   int mode;
@@ -40,11 +45,13 @@ struct FwdParams {
   const int64_t* y;      // labels of this chunk
   float2* partials;      // [rows, ntiles_v] (max, sum-exp)
   float* ztgt;           // [rows] logit of the label
-  float* ref;            // [rows] row reference (FWD_REF output)
+  float* ref;            // [rows] row reference (FWD_REF output, FWD_STATS_P input)
   const float* lse;      // [rows] (FWD_GRAD input)
-  __nv_bfloat16* P;      // [rows, ldp] gradient tile output (FWD_GRAD)
+  __nv_bfloat16* P;      // [rows, ldp] exp tile (FWD_STATS_P) or gradient tile (FWD_GRAD)
   long long ldp;
   int* flags;
+  int* guard;            // FWD_STATS_P: set to 1 if some logit exceeds its row reference + guard
+  const int* only_if;    // if non-null, the launch does nothing unless *only_if != 0
 };
 
 struct DhParams {
@@ -71,7 +78,8 @@ struct GemmGeomHost {
 
 // Kernel launches (return cudaGetLastError()).
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
-                           long long n_override, const float* grad_loss, DevStatus* st, cudaStream_t s);
+                           long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
+                           cudaStream_t s);
 cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
                             const FwdParams& p, int num_sms, cudaStream_t s);
 cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
@@ -80,6 +88,11 @@ cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const Gem
                            const DwParams& p, int* flags, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
+cudaError_t launch_combine_exp(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+                               int V, long long ignore_index, const float* ref, const int* guard, float* lse,
+                               float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s);
+cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, int d, __nv_bfloat16* Ht,
+                          cudaStream_t s);
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
 
 // GEMM tile geometry (must match the kernels).

@@ -23,6 +23,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Logits epilogue. Each thread owns one row of the 128 x 256 tile.
 //   FWD_STATS: per (row, vocab tile) running max m and sum of exp(z - m) over
 //              the tile's in-vocabulary columns, plus the label's logit.
+//   FWD_STATS_P: FWD_STATS, and the exp tile P = bf16(exp(z - ref_row)) for
+//              the backward, where ref_row is the row's maximum over the first
+//              vocabulary tile; sets the chunk's guard word if a logit exceeds
+//              ref_row by more than kRefGuardNats (bf16 range protection).
 //   FWD_REF:   the row maximum over the tile (launched for tile 0 only).
 //   FWD_GRAD:  the gradient tile exp(z - lse) - [v = y] in bf16 for valid rows,
 //              zeros for ignored rows and for columns past the vocabulary.
@@ -30,6 +34,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct FwdEpi {
   using Params = FwdParams;
   struct State {};
+  static __device__ __forceinline__ bool skip(const Params& p) { return p.only_if != nullptr && *p.only_if == 0; }
   static __device__ __forceinline__ void init(const Params&, State&) {}
 
   static __device__ __forceinline__ void tile(const Params& p, State&, int m0, int n0, int row, uint32_t taddr) {
@@ -44,8 +49,12 @@ struct FwdEpi {
       grad_tile(p, r, live, valid, ycol, vlim, n0, taddr);
       return;
     }
+    const bool store_p = p.mode == FWD_STATS_P;
+    const float refv = (store_p && live) ? p.ref[r] : 0.f;
+    const float rb = refv * kLog2e;
+    __nv_bfloat16* dst = p.P + static_cast<long long>(r) * p.ldp + n0;
     float m = -INFINITY, s = 0.f, zt = 0.f;
-    bool have_t = false;
+    bool have_t = false, over = false;
 #pragma unroll 1
     for (int j = 0; j < BN / 32; ++j) {
       float v[32];
@@ -55,7 +64,7 @@ struct FwdEpi {
 #pragma unroll
       for (int c = 0; c < 32; ++c)
         if (c0 + c < vlim) cm = fmaxf(cm, v[c]);
-      if (p.mode == FWD_STATS) {
+      if (p.mode != FWD_REF) {
         if (cm > m) {
           s *= exp2f((m - cm) * kLog2e);
           m = cm;
@@ -70,12 +79,26 @@ struct FwdEpi {
             zt = v[c];
             have_t = true;
           }
+        if (store_p && live) {
+          over |= cm > refv + kRefGuardNats;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float e0 = (c0 + c < vlim) ? exp2f(fmaf(v[c], kLog2e, -rb)) : 0.f;
+            const float e1 = (c0 + c + 1 < vlim) ? exp2f(fmaf(v[c + 1], kLog2e, -rb)) : 0.f;
+            pk[c / 2] = pack_bf16x2(e0, e1);
+          }
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
       } else {
         m = fmaxf(m, cm);
       }
     }
     if (!live) return;
-    if (p.mode == FWD_STATS) {
+    if (over) *p.guard = 1;
+    if (p.mode != FWD_REF) {
       p.partials[static_cast<long long>(r) * p.ntiles_v + n0 / BN] = make_float2(m, s);
       if (have_t) p.ztgt[r] = zt;
     } else {
@@ -116,6 +139,7 @@ struct DhEpi {
   struct State {
     float g;
   };
+  static __device__ __forceinline__ bool skip(const Params&) { return false; }
   static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
@@ -151,6 +175,7 @@ struct DwEpi {
   struct State {
     float g;
   };
+  static __device__ __forceinline__ bool skip(const Params&) { return false; }
   static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
@@ -186,7 +211,8 @@ struct DwEpi {
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k_prepare(const int64_t* __restrict__ y, long long N, int V,
                                                   long long ignore_index, int reduction, long long n_override,
-                                                  const float* grad_loss, DevStatus* st) {
+                                                  const float* grad_loss, DevStatus* st, int* guards, int nguards) {
+  for (int i = threadIdx.x; i < nguards; i += blockDim.x) guards[i] = 0;
   __shared__ long long s_cnt[32];
   __shared__ int s_bad[32];
   long long cnt = 0;
@@ -270,6 +296,72 @@ __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ part
   }
 }
 
+// k_combine, plus what the backward needs from the exp tile P = exp(z - ref):
+// alpha_i = exp(ref_i - lse_i) for valid rows (so that alpha_i P_iv is the
+// softmax) and the label entry rewritten as exp(z_y - ref) - exp(lse - ref)
+// (so that alpha_i P_iy = p_iy - 1). Ignored rows get alpha = 0. If the
+// chunk's guard tripped, the exact gradient tile replaces P and alpha is 1.
+__global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ partials, int T, int rows,
+                                                     const float* __restrict__ ztgt, const int64_t* __restrict__ y,
+                                                     int V, long long ignore_index, const float* __restrict__ ref,
+                                                     const int* __restrict__ guard, float* __restrict__ lse,
+                                                     float* __restrict__ loss_i, float* __restrict__ alpha,
+                                                     __nv_bfloat16* __restrict__ P, long long ldp) {
+  const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float m = -INFINITY, s = 0.f;
+  const float2* pr = partials + static_cast<long long>(r) * T;
+  for (int t = lane; t < T; t += 32) {
+    const float2 q = pr[t];
+    merge_ms(m, s, q.x, q.y);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_ms(m, s, m2, s2);
+  }
+  if (lane == 0) {
+    const float l = m + logf(s);
+    lse[r] = l;
+    const long long yr = y[r];
+    const bool valid = yr != ignore_index && yr >= 0 && yr < V;
+    loss_i[r] = valid ? l - ztgt[r] : 0.f;
+    float a = 0.f;
+    if (valid) {
+      if (*guard != 0) {
+        a = 1.f;
+      } else {
+        const float rf = ref[r];
+        a = exp2f((rf - l) * kLog2e);
+        const float py = exp2f((ztgt[r] - rf) * kLog2e) - exp2f((l - rf) * kLog2e);
+        P[static_cast<long long>(r) * ldp + yr] = __float2bfloat16_rn(py);
+      }
+    }
+    alpha[r] = a;
+  }
+}
+
+// Ht_r = bf16(alpha_r * H_r): the per-row softmax scale moved onto the dW
+// GEMM's B operand (dW = P^T Ht). Eight bf16 per thread; d % 8 == 0.
+__global__ void __launch_bounds__(256) k_hscale(const uint4* __restrict__ H, const float* __restrict__ alpha,
+                                                long long groups, int groups_per_row, uint4* __restrict__ Ht) {
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < groups;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float a = alpha[i / groups_per_row];
+    const uint4 h = H[i];
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(w[q] << 16) * a;
+      const float hi = __uint_as_float(w[q] & 0xffff0000u) * a;
+      o[q] = pack_bf16x2(lo, hi);
+    }
+    Ht[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
 // loss = (sum_i loss_i) * lscale, fp64 accumulation in a fixed order.
 __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ loss_i, long long N,
                                                    const DevStatus* st, float* loss) {
@@ -325,8 +417,9 @@ cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const Gem
 }
 
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
-                           long long n_override, const float* grad_loss, DevStatus* st, cudaStream_t s) {
-  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st);
+                           long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
+                           cudaStream_t s) {
+  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st, guards, nguards);
   return cudaGetLastError();
 }
 
@@ -336,6 +429,28 @@ cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
   k_combine<<<grid, 32 * warps_per_block, 0, s>>>(partials, ntiles_v, rows, ztgt, y, V, ignore_index, lse, loss_i);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_exp(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+                               int V, long long ignore_index, const float* ref, const int* guard, float* lse,
+                               float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps_per_block = 8;
+  const int grid = (rows + warps_per_block - 1) / warps_per_block;
+  k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, ntiles_v, rows, ztgt, y, V, ignore_index, ref, guard,
+                                                       lse, loss_i, alpha, P, ldp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, int d, __nv_bfloat16* Ht,
+                          cudaStream_t s) {
+  const long long groups = static_cast<long long>(rows) * (d / 8);
+  if (groups <= 0) return cudaSuccess;
+  long long blocks = (groups + 255) / 256;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  k_hscale<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(H), alpha, groups, d / 8,
+                                                    reinterpret_cast<uint4*>(Ht));
   return cudaGetLastError();
 }
 

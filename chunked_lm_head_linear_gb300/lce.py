@@ -36,7 +36,7 @@ LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
 EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
             "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc")
-LCE_KERNEL_KINDS = 8
+LCE_KERNEL_KINDS = 10
 
 
 class LceOpts(ctypes.Structure):

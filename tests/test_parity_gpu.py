@@ -122,6 +122,23 @@ def test_large_logits_and_zipf_labels(cuda_lib):
     check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
 
 
+def test_reference_guard_falls_back_to_exact_gradient(cuda_lib):
+    """The fused call stores exp(z - ref) with ref = the row's maximum over the
+    first 256 words. A word outside that tile whose logits reach ~80 sigma
+    above it trips the guard; the chunk must then use the exact gradient tile
+    and still match the oracle."""
+    inp = small_inputs(300, 64, 1000, seed=17, sigma_w=0.05)
+    W = inputs.bf16_bits_to_f32(inp["W"]).astype(np.float64)
+    W[700] = 10.0                                  # z_{i,700} = 10 * sum_k H_ik ~ N(0, 80^2)
+    inp["W"] = inputs.f64_to_bf16_bits(W)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    assert np.max(ref["lse"]) > 100
+    H, Wd, y = to_dev(inp)
+    for chunk in (0, 128):
+        loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, Wd, y, chunk_tokens=chunk, sync_check=True)
+        check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
 def test_reduction_sum_grad_scale_and_override(cuda_lib):
     torch = _torch()
     inp = small_inputs(300, 128, 1500, seed=9)
@@ -200,7 +217,7 @@ def test_chunk_size_invariance_and_determinism(cuda_lib):
         assert torch.equal(o[0], base[0]), C
         assert torch.equal(o[1], base[1]), C
         assert torch.equal(o[2], base[2]), C
-        assert rel_fro(o[3].cpu().numpy(), base[3].cpu().numpy()) <= 1e-6, C
+        assert rel_fro(o[3].cpu().numpy(), base[3].cpu().numpy()) <= TOL_DW_CHUNKING, C
         check_against_oracle(ref, inp["y"], o[0].item(), o[1].cpu().numpy(), bf16_to_np(o[2]), o[3].cpu().numpy())
     again = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=128, sync_check=True)
     for a, b in zip(again, base):
@@ -286,10 +303,20 @@ def test_full_moe_workloads(cuda_lib, name):
     sampled_full_check(cuda_lib, name)
 
 
+# dW is summed over chunks in fp32. Changing the chunking reassociates that sum
+# (and the GEMM's own K order): with n_c chunk partials the recursive-summation
+# bound is n_c * 2^-24 * sum|partials| per element, and the softmax and one-hot
+# parts of each partial partly cancel (sum|partials| ~ 2 |dW|). For two chunkings
+# with at most 64 chunks: 2 * 64 * 2^-24 * 2 ~ 1.5e-5 worst case; 1e-5 is used
+# (measured 1.5e-6 between 8 and 64 chunks).
+TOL_DW_CHUNKING = 1e-5
+
+
 @pytest.mark.slow
 def test_full_seq64k_chunk_sweep(cuda_lib):
     """64k-token head, chunk sizes 1024..8192: every chunk size within the oracle
-    tolerance; lse and dH bitwise equal across chunk sizes; dW within 1e-6."""
+    tolerance; loss, lse and dH bitwise equal across chunk sizes; dW within the
+    fp32 reassociation bound TOL_DW_CHUNKING."""
     torch = _torch()
     name = "seq64k_n65536_d4096_v151936"
     first = None
@@ -299,6 +326,6 @@ def test_full_seq64k_chunk_sweep(cuda_lib):
             first = (loss.clone(), lse.clone(), dH.clone(), dW.clone())
         else:
             assert torch.equal(loss, first[0]) and torch.equal(lse, first[1]) and torch.equal(dH, first[2])
-            assert ((dW - first[3]).norm() / first[3].norm()).item() <= 1e-6
+            assert ((dW - first[3]).norm() / first[3].norm()).item() <= TOL_DW_CHUNKING
         del loss, lse, dH, dW
         torch.cuda.empty_cache()
