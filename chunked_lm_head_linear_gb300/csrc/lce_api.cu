@@ -93,7 +93,7 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
   if (fwd) {
     L.loss_i = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
     L.ztgt = take(sizeof(float) * static_cast<size_t>(L.C));
-    L.partials = take(sizeof(float) * 2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.T));
+    L.partials = take(sizeof(float) * 2 * static_cast<size_t>(L.C) * static_cast<size_t>(2 * L.T));
   }
   L.chunks = N > 0 ? ceil_div(N, L.C) : 0;
   if (op == LCE_OP_FWD_BWD) {
@@ -139,19 +139,28 @@ int device_check(DeviceInfo* info) {
   return LCE_OK;
 }
 
-// 2-D bf16 tensor map over a row-major [rows, cols] matrix with row stride ld
-// (elements), 128-byte swizzle, box = {64 columns, box_rows rows}. Reads past
-// rows/cols return zeros.
-int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+// 2-D tensor map over a row-major [rows, cols] matrix with row stride ld
+// (elements), 128-byte swizzle, box = {box_cols, box_rows} (box_cols * element
+// size = 128 bytes). Loads past rows/cols return zeros; stores there are dropped.
+int make_map_t(CUtensorMap* m, CUtensorMapDataType dtype, uint32_t esize, const void* base, int64_t rows,
+               int64_t cols, int64_t ld, uint32_t box_cols, uint32_t box_rows) {
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {64u, box_rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r = encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                                 estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  const CUresult r = encode_fn()(m, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+                                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? LCE_OK : LCE_ERR_CUDA;
 }
+
+// bf16 operand / output map: boxes of 64 columns.
+int make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int64_t ld, uint32_t box_rows) {
+  return make_map_t(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, cols, ld, 64u, box_rows);
+}
+
+// Rows of output tile one epilogue warp stores at a time.
+constexpr uint32_t kStoreRows = 32;
 
 #define LCE_TRY(x)                         \
   do {                                     \
@@ -247,9 +256,13 @@ struct LogitsArgs {
 };
 
 int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
-  CUtensorMap mA, mB;
+  CUtensorMap mA, mB, mC;
   LCE_TRY(make_map(&mA, c.H + c0 * c.d, rows, c.d, c.d, lce::kTileM));
   LCE_TRY(make_map(&mB, c.W, c.V, c.d, c.d, lce::kTileN));
+  if (a.P)  // exp / gradient tile: [rows, V] bf16 with row stride ldp
+    LCE_TRY(make_map(&mC, a.P, rows, c.V, c.L.ldp, kStoreRows));
+  else
+    mC = mB;  // this epilogue stores nothing
   const int n_tiles = a.mode == lce::FWD_REF ? 1 : static_cast<int>(c.L.T);
   lce::GemmGeomHost g{static_cast<int>(ceil_div(rows, lce::kTileM)), n_tiles,
                       static_cast<int>(ceil_div(c.d, lce::kTileK)), 1};
@@ -258,7 +271,7 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   p.mode = a.mode;
   p.rows = static_cast<int>(rows);
   p.V = static_cast<int>(c.V);
-  p.ntiles_v = static_cast<int>(c.L.T);
+  p.nparts = static_cast<int>(2 * c.L.T);
   p.ignore_index = c.o.ignore_index;
   p.y = c.y + c0;
   p.partials = reinterpret_cast<float2*>(c.ws + c.L.partials);
@@ -276,16 +289,16 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   if (a.mode == lce::FWD_REF) kind = K_LOGITS_REF;
   if (a.mode == lce::FWD_GRAD) kind = a.only_if ? K_OTHER : K_LOGITS_GRAD;
   return timed(c.s, kind, a.only_if ? 0.0 : flops,
-               [&] { return cuda_rc(lce::launch_fwd_gemm(mA, mB, g, p, c.dev.num_sms, c.s)); });
+               [&] { return cuda_rc(lce::launch_fwd_gemm(mA, mB, mC, g, p, c.dev.num_sms, c.s)); });
 }
 
 int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* loss_i) {
   LogitsArgs a;
   a.mode = lce::FWD_STATS;
   LCE_TRY(logits_gemm(c, c0, rows, a));
-  const double bytes = static_cast<double>(rows) * (8.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4);
+  const double bytes = static_cast<double>(rows) * (16.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4);
   return timed(c.s, K_COMBINE, bytes, [&] {
-    return cuda_rc(lce::launch_combine(reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(c.L.T),
+    return cuda_rc(lce::launch_combine(reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(2 * c.L.T),
                                        static_cast<int>(rows), reinterpret_cast<const float*>(c.ws + c.L.ztgt),
                                        c.y + c0, static_cast<int>(c.V), c.o.ignore_index, lse + c0, loss_i + c0,
                                        c.s));
@@ -300,9 +313,10 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
 
   // dH_c: A = G_c [rows, V] K-major, B = W [V, d] read N-major.
-  CUtensorMap mG, mW;
+  CUtensorMap mG, mW, mdH;
   LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kTileM));
   LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, 64));
+  LCE_TRY(make_map(&mdH, dH + c0 * c.d, rows, c.d, c.d, kStoreRows));
   lce::GemmGeomHost gh{static_cast<int>(ceil_div(rows, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
                        static_cast<int>(ceil_div(c.V, lce::kTileK)), 0};
   lce::DhParams dp;
@@ -313,12 +327,13 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   dp.rowscale = rowscale;
   dp.st = c.st;
   LCE_TRY(timed(c.s, K_GEMM_DH, flops,
-                [&] { return cuda_rc(lce::launch_dh_gemm(mG, mW, gh, dp, &c.st->flags, c.dev.num_sms, c.s)); }));
+                [&] { return cuda_rc(lce::launch_dh_gemm(mG, mW, mdH, gh, dp, &c.st->flags, c.dev.num_sms, c.s)); }));
 
   // dW: A = G_c^T (G_c read M-major), B = [rows, d] read N-major.
-  CUtensorMap mGt, mB;
+  CUtensorMap mGt, mB, mdW;
   LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, 64));
   LCE_TRY(make_map(&mB, B, rows, c.d, c.d, 64));
+  LCE_TRY(make_map_t(&mdW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, c.V, c.d, c.d, 32u, kStoreRows));
   lce::GemmGeomHost gw{static_cast<int>(ceil_div(c.V, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
                        static_cast<int>(ceil_div(rows, lce::kTileK)), 0};
   lce::DwParams wp;
@@ -329,7 +344,7 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   wp.accumulate = accumulate ? 1 : 0;
   wp.st = c.st;
   return timed(c.s, K_GEMM_DW, flops,
-               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mB, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
+               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mB, mdW, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
 }
 
 // Backward of one chunk from a known lse: recompute the logits into the
@@ -364,10 +379,10 @@ int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* l
   a.guard = guard;
   LCE_TRY(logits_gemm(c, c0, rows, a));
 
-  const double cbytes = static_cast<double>(rows) * (8.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2);
+  const double cbytes = static_cast<double>(rows) * (16.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2);
   LCE_TRY(timed(c.s, K_COMBINE, cbytes, [&] {
     return cuda_rc(lce::launch_combine_exp(reinterpret_cast<const float2*>(c.ws + c.L.partials),
-                                           static_cast<int>(c.L.T), static_cast<int>(rows),
+                                           static_cast<int>(2 * c.L.T), static_cast<int>(rows),
                                            reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0,
                                            static_cast<int>(c.V), c.o.ignore_index, ref, guard, lse + c0, loss_i + c0,
                                            alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp, c.s));

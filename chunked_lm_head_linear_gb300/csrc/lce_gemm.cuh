@@ -8,11 +8,15 @@
 // ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation", section 3.1.4:
 // the logits chunk, and the backward's d_input / d_weight.)
 //
-// One CTA per SM, 256 threads:
-//   warp 0     TMA producer (one thread): A/B k-blocks into a STAGES-deep ring
-//   warp 1     MMA issuer (one thread): tcgen05.mma 128x256x16, fp32 in TMEM
-//   warp 2     TMEM allocator (512 columns = two 128x256 fp32 accumulators)
-//   warps 4-7  epilogue: TMEM -> registers -> per-tile arithmetic -> global
+// One CTA per SM, 384 threads:
+//   warp 0      TMA producer (one thread): A/B k-blocks into a STAGES-deep ring
+//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16, fp32 in TMEM
+//   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
+//   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (the hardware
+//               lane quarter of its sub-partition) and columns
+//               128*((w-4)/4).. of the tile, does the per-tile arithmetic and
+//               writes results through its own 4 KiB shared-memory staging
+//               tile with TMA stores (or TMA reduce-adds).
 // The two accumulators alternate so the epilogue of tile t overlaps the main
 // loop of tile t+1. Tiles are assigned statically: tile = blockIdx.x + i*grid.
 #pragma once
@@ -29,8 +33,11 @@ constexpr int STAGES = 4;
 constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
 constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int MN_SLAB_BYTES = 64 * BK * 2;   // one 64-wide MN slab of a k-block: 8 KiB
-constexpr int NUM_THREADS = 256;
 constexpr int EPI_WARP0 = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_COLS = BN / 2;             // columns of the tile one epilogue warp owns
+constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
+constexpr int STAGE_TILE_BYTES = 4096;       // 32 rows x 128 bytes, 128-byte swizzled
 constexpr int TMEM_COLS = 2 * BN;
 
 struct GemmGeom {
@@ -41,12 +48,47 @@ struct GemmGeom {
 
 struct SmemLayout {
   static constexpr int kTiles = STAGES * (A_STAGE_BYTES + B_STAGE_BYTES);
-  static constexpr int kBars = kTiles;                  // mbarriers after the tiles
+  static constexpr int kStaging = kTiles;                          // EPI_WARPS staging tiles
+  static constexpr int kBars = kStaging + EPI_WARPS * STAGE_TILE_BYTES;
   static constexpr int kNumBars = 2 * STAGES + 4 + 1;   // full, empty, tmem_full[2], tmem_empty[2], drain
   static constexpr int kMisc = kBars + kNumBars * 8;    // tmem holder + abort flag
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kDynamicBytes = kTotal + 1024;   // slack for 1 KiB alignment
 };
+static_assert(SmemLayout::kDynamicBytes <= 232448, "shared memory budget");
+
+// What an epilogue warp needs besides its tile: its staging tile, the store
+// map and where its 32 rows start.
+struct EpiCtx {
+  uint8_t* stage;            // this warp's staging tile (1 KiB aligned)
+  const CUtensorMap* out;    // TMA store / reduce map of the epilogue's output
+  int lane;
+  int row0;                  // first tile row of this warp (tile-relative)
+};
+
+// Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled staging tile.
+__device__ __forceinline__ uint32_t stage_off(int r, int j) {
+  return static_cast<uint32_t>(r * 128 + ((j ^ (r & 7)) << 4));
+}
+
+// Before rewriting the staging tile: the previous TMA store must have read it.
+__device__ __forceinline__ void stage_acquire(const EpiCtx& c) {
+  if (c.lane == 0) bulk_wait_read_all();
+  __syncwarp();
+}
+
+// Hand the staging tile to TMA: store (or add) it at element (x, y) of the output.
+__device__ __forceinline__ void stage_release(const EpiCtx& c, int x, int y, bool reduce_add) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (c.lane == 0) {
+    if (reduce_add)
+      tma_reduce_add_2d(c.out, c.stage, x, y);
+    else
+      tma_store_2d(c.out, c.stage, x, y);
+    bulk_commit();
+  }
+}
 
 __device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& m_blk, int& n_blk) {
   if (g.m_fast) {
@@ -73,8 +115,8 @@ __device__ __forceinline__ void report_timeout(volatile int* abort, int* flags) 
 
 template <bool A_MN, bool B_MN, class Epi>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmGeom g,
-                typename Epi::Params ep) {
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmC, GemmGeom g, typename Epi::Params ep) {
   if (Epi::skip(ep)) return;  // conditional launch whose condition is false: no work at all
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -82,6 +124,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint8_t* staging = smem + SmemLayout::kStaging;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBars);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
@@ -102,7 +145,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 32 * EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort = 0;
@@ -221,8 +264,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp >= EPI_WARP0) {
     // ---------------- epilogue ----------------
-    const int q = warp - EPI_WARP0;   // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;    // row of the output tile
+    const int e = warp - EPI_WARP0;   // 0 .. EPI_WARPS-1
+    const int q = warp & 3;           // TMEM lane quarter this warp may access
+    const int half = e >> 2;          // which 128 columns of the tile
+    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, &tmC, lane, q * 32};
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Epi::State st;
@@ -235,8 +280,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_after_sync();
       int mb, nb;
       tile_coords(g, t, mb, nb);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      Epi::tile(ep, st, mb * BM, nb * BN, row, taddr);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN + half * EPI_COLS);
+      Epi::tile(ep, st, ctx, mb * BM, nb * BN + half * EPI_COLS, taddr);
       tc_fence_before_sync();
       mbar_arrive(&tempty[acc]);
       if (++acc == 2) {
@@ -244,6 +290,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc_phase ^= 1u;
       }
     }
+    if (lane == 0) bulk_wait_all();   // every store of this warp has landed
+    __syncwarp();
   }
 
   tc_fence_before_sync();

@@ -40,10 +40,10 @@ struct FwdParams {
   int mode;
   int rows;              // rows of this chunk
   int V;
-  int ntiles_v;          // vocabulary tiles per row (partials row stride)
+  int nparts;            // partials per row: two per 256-column vocabulary tile
   long long ignore_index;
   const int64_t* y;      // labels of this chunk
-  float2* partials;      // [rows, ntiles_v] (max, sum-exp)
+  float2* partials;      // [rows, nparts] (max, sum-exp) per 128-column half tile
   float* ztgt;           // [rows] logit of the label
   float* ref;            // [rows] row reference (FWD_REF output, FWD_STATS_P input)
   const float* lse;      // [rows] (FWD_GRAD input)
@@ -80,15 +80,16 @@ struct GemmGeomHost {
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
                            long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
                            cudaStream_t s);
-cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+// a, b: operand tensor maps; c: the epilogue's TMA store map (any valid map if unused).
+cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
                             const FwdParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
                            const DhParams& p, int* flags, int num_sms, cudaStream_t s);
-cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g,
+cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
                            const DwParams& p, int* flags, int num_sms, cudaStream_t s);
-cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+cudaError_t launch_combine(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
-cudaError_t launch_combine_exp(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s);
 cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, int d, __nv_bfloat16* Ht,

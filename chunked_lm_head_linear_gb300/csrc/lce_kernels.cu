@@ -20,16 +20,21 @@ namespace lce {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ----------------------------------------------------------------------------
-// Logits epilogue. Each thread owns one row of the 128 x 256 tile.
-//   FWD_STATS: per (row, vocab tile) running max m and sum of exp(z - m) over
-//              the tile's in-vocabulary columns, plus the label's logit.
-//   FWD_STATS_P: FWD_STATS, and the exp tile P = bf16(exp(z - ref_row)) for
-//              the backward, where ref_row is the row's maximum over the first
-//              vocabulary tile; sets the chunk's guard word if a logit exceeds
-//              ref_row by more than kRefGuardNats (bf16 range protection).
-//   FWD_REF:   the row maximum over the tile (launched for tile 0 only).
-//   FWD_GRAD:  the gradient tile exp(z - lse) - [v = y] in bf16 for valid rows,
-//              zeros for ignored rows and for columns past the vocabulary.
+// Logits epilogue. An epilogue warp owns 32 rows x 128 columns of the 128 x 256
+// tile (one thread = one row); results leave through the warp's swizzled
+// staging tile as TMA stores of 32 rows x 64 bf16.
+//   FWD_STATS:   per (row, 128-column half tile) max m and sum of exp(z - m)
+//                over the in-vocabulary columns, plus the label's logit.
+//   FWD_STATS_P: FWD_STATS, and the exp tile P = bf16(exp(z - ref_row)) for the
+//                backward, where ref_row is the row's maximum over the first
+//                128 words; sets the chunk's guard word if a logit exceeds
+//                ref_row by more than kRefGuardNats (bf16 range protection).
+//   FWD_REF:     ref_row (launched for the first tile only; the warps holding
+//                columns 128..255 do nothing).
+//   FWD_GRAD:    the gradient tile exp(z - lse) - [v = y] in bf16 for valid
+//                rows, zeros for ignored rows.
+// Columns past the vocabulary are masked to -inf (zero logits are not neutral
+// in a softmax); stores past the vocabulary are dropped by TMA.
 // ----------------------------------------------------------------------------
 struct FwdEpi {
   using Params = FwdParams;
@@ -37,103 +42,107 @@ struct FwdEpi {
   static __device__ __forceinline__ bool skip(const Params& p) { return p.only_if != nullptr && *p.only_if == 0; }
   static __device__ __forceinline__ void init(const Params&, State&) {}
 
-  static __device__ __forceinline__ void tile(const Params& p, State&, int m0, int n0, int row, uint32_t taddr) {
-    const int r = m0 + row;
+  static __device__ __forceinline__ void tile(const Params& p, State&, const EpiCtx& ctx, int m0, int col0,
+                                              uint32_t taddr) {
+    const int lane = ctx.lane;
+    const int r = m0 + ctx.row0 + lane;
     const bool live = r < p.rows;
     const long long yr = live ? static_cast<long long>(p.y[r]) : p.ignore_index;
     const bool valid = live && yr != p.ignore_index && yr >= 0 && yr < p.V;
-    const int ycol = valid ? static_cast<int>(yr - n0) : -1;
-    const int vlim = p.V - n0;  // columns >= vlim are past the vocabulary
+    const int ycol = valid ? static_cast<int>(yr - col0) : -1;
+    const int vlim = p.V - col0;  // columns >= vlim are past the vocabulary (warp-uniform)
+    const int part = col0 / EPI_COLS;
 
-    if (p.mode == FWD_GRAD) {
-      grad_tile(p, r, live, valid, ycol, vlim, n0, taddr);
+    if (p.mode == FWD_REF && col0 >= EPI_COLS) return;
+    if (vlim <= 0) {  // this half tile lies entirely past the vocabulary
+      if (live && p.mode != FWD_REF && p.mode != FWD_GRAD)
+        p.partials[static_cast<long long>(r) * p.nparts + part] = make_float2(-INFINITY, 0.f);
       return;
     }
-    const bool store_p = p.mode == FWD_STATS_P;
-    const float refv = (store_p && live) ? p.ref[r] : 0.f;
+    const bool grad = p.mode == FWD_GRAD;
+    const bool stats = p.mode == FWD_STATS || p.mode == FWD_STATS_P;
+    const bool store = p.mode == FWD_STATS_P || grad;
+    const float refv = !live ? 0.f : (grad ? p.lse[r] : (p.mode == FWD_STATS_P ? p.ref[r] : 0.f));
     const float rb = refv * kLog2e;
-    __nv_bfloat16* dst = p.P + static_cast<long long>(r) * p.ldp + n0;
+    const float gmask = (grad && !valid) ? 0.f : 1.f;   // gradient rows of ignored tokens are zero
+
+    // A store box never starts past the output's extent (rows or vocabulary).
+    const bool rows_in = m0 + ctx.row0 < p.rows;
     float m = -INFINITY, s = 0.f, zt = 0.f;
     bool have_t = false, over = false;
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
-      float v[32];
-      tmem_ld_32x32b_x32(taddr + j * 32, v);
-      const int c0 = j * 32;
-      float cm = -INFINITY;
+    for (int u = 0; u < EPI_COLS / 64; ++u) {
+      if (u * 64 >= vlim) break;  // the rest of this half tile is past the vocabulary
+      if (store) stage_acquire(ctx);
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const int c0 = u * 64 + hh * 32;
+        float v[32];
+        tmem_ld_32x32b_x32(taddr + c0, v);
+        if (vlim < c0 + 32) {
 #pragma unroll
-      for (int c = 0; c < 32; ++c)
-        if (c0 + c < vlim) cm = fmaxf(cm, v[c]);
-      if (p.mode != FWD_REF) {
-        if (cm > m) {
-          s *= exp2f((m - cm) * kLog2e);
-          m = cm;
+          for (int c = 0; c < 32; ++c)
+            if (c0 + c >= vlim) v[c] = -INFINITY;
         }
-        const float mb = m * kLog2e;
+        if (stats || p.mode == FWD_REF) {
+          float cm = v[0];
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c0 + c < vlim) s += exp2f(fmaf(v[c], kLog2e, -mb));
+          for (int c = 1; c < 32; ++c) cm = fmaxf(cm, v[c]);
+          if (p.mode == FWD_REF) {
+            m = fmaxf(m, cm);
+          } else {
+            if (cm > m) {
+              s *= ex2_approx((m - cm) * kLog2e);
+              m = cm;
+            }
+            const float mb = m * kLog2e;
+            float s2 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c)
-          if (c0 + c == ycol) {
-            zt = v[c];
-            have_t = true;
+            for (int c = 0; c < 32; ++c) s2 += ex2_approx(fmaf(v[c], kLog2e, -mb));
+            s += s2;
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c0 + c == ycol) {
+                zt = v[c];
+                have_t = true;
+              }
+            over |= cm > refv + kRefGuardNats;
           }
-        if (store_p && live) {
-          over |= cm > refv + kRefGuardNats;
+        }
+        if (store) {
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
-            const float e0 = (c0 + c < vlim) ? exp2f(fmaf(v[c], kLog2e, -rb)) : 0.f;
-            const float e1 = (c0 + c + 1 < vlim) ? exp2f(fmaf(v[c + 1], kLog2e, -rb)) : 0.f;
+            float e0 = ex2_approx(fmaf(v[c], kLog2e, -rb));
+            float e1 = ex2_approx(fmaf(v[c + 1], kLog2e, -rb));
+            if (grad) {
+              e0 = (e0 - (c0 + c == ycol ? 1.f : 0.f)) * gmask;
+              e1 = (e1 - (c0 + c + 1 == ycol ? 1.f : 0.f)) * gmask;
+            }
             pk[c / 2] = pack_bf16x2(e0, e1);
           }
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(ctx.stage + stage_off(lane, hh * 4 + q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
-      } else {
-        m = fmaxf(m, cm);
       }
+      if (store && rows_in) stage_release(ctx, col0 + u * 64, m0 + ctx.row0, false);
     }
     if (!live) return;
-    if (over) *p.guard = 1;
-    if (p.mode != FWD_REF) {
-      p.partials[static_cast<long long>(r) * p.ntiles_v + n0 / BN] = make_float2(m, s);
-      if (have_t) p.ztgt[r] = zt;
-    } else {
+    if (p.mode == FWD_REF) {
       p.ref[r] = m;
+      return;
     }
-  }
-
-  static __device__ __forceinline__ void grad_tile(const Params& p, int r, bool live, bool valid, int ycol, int vlim,
-                                                   int n0, uint32_t taddr) {
-    const float rb = (live ? p.lse[r] : 0.f) * kLog2e;
-    __nv_bfloat16* dst = p.P + static_cast<long long>(r) * p.ldp + n0;
-#pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
-      float v[32];
-      tmem_ld_32x32b_x32(taddr + j * 32, v);
-      if (!live) continue;
-      const int c0 = j * 32;
-      uint32_t pk[16];
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        float e0 = 0.f, e1 = 0.f;
-        if (valid) {
-          if (c0 + c < vlim) e0 = exp2f(fmaf(v[c], kLog2e, -rb)) - (c0 + c == ycol ? 1.f : 0.f);
-          if (c0 + c + 1 < vlim) e1 = exp2f(fmaf(v[c + 1], kLog2e, -rb)) - (c0 + c + 1 == ycol ? 1.f : 0.f);
-        }
-        pk[c / 2] = pack_bf16x2(e0, e1);
-      }
-      uint4* d4 = reinterpret_cast<uint4*>(dst + c0);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) d4[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    if (stats) {
+      p.partials[static_cast<long long>(r) * p.nparts + part] = make_float2(m, s);
+      if (have_t) p.ztgt[r] = zt;
+      if (p.mode == FWD_STATS_P && over) *p.guard = 1;
     }
   }
 };
 
-// dH tile: bf16(acc * g/n [* per-row factor]) into the chunk's rows of dH.
+// dH tile: bf16(acc * g/n [* per-row factor]), stored by TMA into the chunk's dH rows.
 struct DhEpi {
   using Params = DhParams;
   struct State {
@@ -142,34 +151,37 @@ struct DhEpi {
   static __device__ __forceinline__ bool skip(const Params&) { return false; }
   static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
 
-  static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
-    const int r = m0 + row;
-    const bool live = r < p.rows;
+  static __device__ __forceinline__ void tile(const Params& p, State& st, const EpiCtx& ctx, int m0, int col0,
+                                              uint32_t taddr) {
+    const int r = m0 + ctx.row0 + ctx.lane;
+    if (m0 + ctx.row0 >= p.rows) return;  // all 32 rows of this warp are past the chunk
     float f = st.g;
-    if (live && p.rowscale != nullptr) f *= p.rowscale[r];
-    __nv_bfloat16* dst = p.out + static_cast<long long>(r) * p.ld + n0;
+    if (r < p.rows && p.rowscale != nullptr) f *= p.rowscale[r];
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
-      float v[32];
-      tmem_ld_32x32b_x32(taddr + j * 32, v);
-      if (!live) continue;
-      const int c0 = j * 32;
+    for (int u = 0; u < EPI_COLS / 64; ++u) {
+      if (col0 + u * 64 >= p.N) break;
+      stage_acquire(ctx);
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        float v[32];
+        tmem_ld_32x32b_x32(taddr + u * 64 + hh * 32, v);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (n0 + c0 + 8 * q < p.N) {
+        for (int q = 0; q < 4; ++q) {
           uint4 w;
           w.x = pack_bf16x2(v[8 * q + 0] * f, v[8 * q + 1] * f);
           w.y = pack_bf16x2(v[8 * q + 2] * f, v[8 * q + 3] * f);
           w.z = pack_bf16x2(v[8 * q + 4] * f, v[8 * q + 5] * f);
           w.w = pack_bf16x2(v[8 * q + 6] * f, v[8 * q + 7] * f);
-          *reinterpret_cast<uint4*>(dst + c0 + 8 * q) = w;
+          *reinterpret_cast<uint4*>(ctx.stage + stage_off(ctx.lane, hh * 4 + q)) = w;
         }
       }
+      stage_release(ctx, col0 + u * 64, m0 + ctx.row0, false);
     }
   }
 };
 
-// dW tile: fp32 (acc * g/n) stored into, or added to, the vocabulary rows of dW.
+// dW tile: fp32 acc * g/n, stored (first chunk) or added (TMA reduce-add in L2)
+// into the vocabulary rows of dW.
 struct DwEpi {
   using Params = DwParams;
   struct State {
@@ -178,29 +190,21 @@ struct DwEpi {
   static __device__ __forceinline__ bool skip(const Params&) { return false; }
   static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
 
-  static __device__ __forceinline__ void tile(const Params& p, State& st, int m0, int n0, int row, uint32_t taddr) {
-    const int r = m0 + row;
-    const bool live = r < p.rows;
+  static __device__ __forceinline__ void tile(const Params& p, State& st, const EpiCtx& ctx, int m0, int col0,
+                                              uint32_t taddr) {
     const float f = st.g;
-    float* dst = p.out + static_cast<long long>(r) * p.ld + n0;
+    if (m0 + ctx.row0 >= p.rows) return;  // all 32 rows of this warp are past the vocabulary
 #pragma unroll 1
-    for (int j = 0; j < BN / 32; ++j) {
+    for (int u = 0; u < EPI_COLS / 32; ++u) {
+      if (col0 + u * 32 >= p.N) break;
+      stage_acquire(ctx);
       float v[32];
-      tmem_ld_32x32b_x32(taddr + j * 32, v);
-      if (!live) continue;
-      const int c0 = j * 32;
+      tmem_ld_32x32b_x32(taddr + u * 32, v);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (n0 + c0 + 4 * q < p.N) {
-          float4* a = reinterpret_cast<float4*>(dst + c0 + 4 * q);
-          float4 o = p.accumulate ? *a : make_float4(0.f, 0.f, 0.f, 0.f);
-          o.x += v[4 * q + 0] * f;
-          o.y += v[4 * q + 1] * f;
-          o.z += v[4 * q + 2] * f;
-          o.w += v[4 * q + 3] * f;
-          *a = o;
-        }
-      }
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<float4*>(ctx.stage + stage_off(ctx.lane, q)) =
+            make_float4(v[4 * q] * f, v[4 * q + 1] * f, v[4 * q + 2] * f, v[4 * q + 3] * f);
+      stage_release(ctx, col0 + u * 32, m0 + ctx.row0, p.accumulate != 0);
     }
   }
 };
@@ -383,8 +387,9 @@ __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ los
 int gemm_smem_bytes() { return SmemLayout::kDynamicBytes; }
 
 template <bool A_MN, bool B_MN, class Epi>
-static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& gh,
-                               const typename Epi::Params& ep, int* flags, int num_sms, cudaStream_t s) {
+static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                               const GemmGeomHost& gh, const typename Epi::Params& ep, int* flags, int num_sms,
+                               cudaStream_t s) {
   auto kern = gemm_kernel<A_MN, B_MN, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::kDynamicBytes);
   if (e != cudaSuccess) return e;
@@ -397,23 +402,23 @@ static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const
   const int tiles = gh.m_tiles * gh.n_tiles;
   if (tiles <= 0) return cudaSuccess;
   const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, NUM_THREADS, SmemLayout::kDynamicBytes, s>>>(a, b, g, ep);
+  kern<<<grid, NUM_THREADS, SmemLayout::kDynamicBytes, s>>>(a, b, c, g, ep);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const FwdParams& p,
-                            int num_sms, cudaStream_t s) {
-  return launch_gemm<false, false, FwdEpi>(a, b, g, p, p.flags, num_sms, s);
+cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
+                            const FwdParams& p, int num_sms, cudaStream_t s) {
+  return launch_gemm<false, false, FwdEpi>(a, b, c, g, p, p.flags, num_sms, s);
 }
 
-cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const DhParams& p,
-                           int* flags, int num_sms, cudaStream_t s) {
-  return launch_gemm<false, true, DhEpi>(a, b, g, p, flags, num_sms, s);
+cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
+                           const DhParams& p, int* flags, int num_sms, cudaStream_t s) {
+  return launch_gemm<false, true, DhEpi>(a, b, c, g, p, flags, num_sms, s);
 }
 
-cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const GemmGeomHost& g, const DwParams& p,
-                           int* flags, int num_sms, cudaStream_t s) {
-  return launch_gemm<true, true, DwEpi>(a, b, g, p, flags, num_sms, s);
+cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
+                           const DwParams& p, int* flags, int num_sms, cudaStream_t s) {
+  return launch_gemm<true, true, DwEpi>(a, b, c, g, p, flags, num_sms, s);
 }
 
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
@@ -423,22 +428,22 @@ cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignor
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+cudaError_t launch_combine(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  k_combine<<<grid, 32 * warps_per_block, 0, s>>>(partials, ntiles_v, rows, ztgt, y, V, ignore_index, lse, loss_i);
+  k_combine<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, lse, loss_i);
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_exp(const float2* partials, int ntiles_v, int rows, const float* ztgt, const int64_t* y,
+cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, ntiles_v, rows, ztgt, y, V, ignore_index, ref, guard,
+  k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, ref, guard,
                                                        lse, loss_i, alpha, P, ldp);
   return cudaGetLastError();
 }
