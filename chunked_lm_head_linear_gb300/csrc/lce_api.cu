@@ -257,15 +257,14 @@ struct LogitsArgs {
 
 int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   CUtensorMap mA, mB, mC;
-  LCE_TRY(make_map(&mA, c.H + c0 * c.d, rows, c.d, c.d, lce::kTileM));
-  LCE_TRY(make_map(&mB, c.W, c.V, c.d, c.d, lce::kTileN));
+  LCE_TRY(make_map(&mA, c.H + c0 * c.d, rows, c.d, c.d, lce::kBoxRowsK));
+  LCE_TRY(make_map(&mB, c.W, c.V, c.d, c.d, lce::kBoxRowsK));
   if (a.P)  // exp / gradient tile: [rows, V] bf16 with row stride ldp
     LCE_TRY(make_map(&mC, a.P, rows, c.V, c.L.ldp, kStoreRows));
   else
     mC = mB;  // this epilogue stores nothing
   const int n_tiles = a.mode == lce::FWD_REF ? 1 : static_cast<int>(c.L.T);
-  lce::GemmGeomHost g{static_cast<int>(ceil_div(rows, lce::kTileM)), n_tiles,
-                      static_cast<int>(ceil_div(c.d, lce::kTileK)), 1};
+  lce::GemmGeomHost g{rows, a.mode == lce::FWD_REF ? lce::kTileN : c.V, c.d, 1};
   lce::FwdParams p;
   std::memset(&p, 0, sizeof p);
   p.mode = a.mode;
@@ -314,11 +313,10 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
 
   // dH_c: A = G_c [rows, V] K-major, B = W [V, d] read N-major.
   CUtensorMap mG, mW, mdH;
-  LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kTileM));
-  LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, 64));
+  LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kBoxRowsK));
+  LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, lce::kBoxRowsMN));
   LCE_TRY(make_map(&mdH, dH + c0 * c.d, rows, c.d, c.d, kStoreRows));
-  lce::GemmGeomHost gh{static_cast<int>(ceil_div(rows, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
-                       static_cast<int>(ceil_div(c.V, lce::kTileK)), 0};
+  lce::GemmGeomHost gh{rows, c.d, c.V, 0};
   lce::DhParams dp;
   dp.rows = static_cast<int>(rows);
   dp.N = static_cast<int>(c.d);
@@ -331,11 +329,10 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
 
   // dW: A = G_c^T (G_c read M-major), B = [rows, d] read N-major.
   CUtensorMap mGt, mB, mdW;
-  LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, 64));
-  LCE_TRY(make_map(&mB, B, rows, c.d, c.d, 64));
+  LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, lce::kBoxRowsMN));
+  LCE_TRY(make_map(&mB, B, rows, c.d, c.d, lce::kBoxRowsMN));
   LCE_TRY(make_map_t(&mdW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, c.V, c.d, c.d, 32u, kStoreRows));
-  lce::GemmGeomHost gw{static_cast<int>(ceil_div(c.V, lce::kTileM)), static_cast<int>(ceil_div(c.d, lce::kTileN)),
-                       static_cast<int>(ceil_div(rows, lce::kTileK)), 0};
+  lce::GemmGeomHost gw{c.V, c.d, rows, 0};
   lce::DwParams wp;
   wp.rows = static_cast<int>(c.V);
   wp.N = static_cast<int>(c.d);

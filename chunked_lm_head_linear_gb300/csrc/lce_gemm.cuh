@@ -300,4 +300,240 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
 }
 
+// ============================================================================
+// CTA-pair variant: tcgen05.mma.cta_group::2, 256 x 256 output tile per pair.
+// Launched with clusters of two CTAs (one TPC). CTA rank r of the pair loads
+// rows [128 r, 128 r + 128) of the A tile and columns [128 r, 128 r + 128) of
+// the B tile into its own shared memory; the even CTA's MMA thread multiplies
+// across both, and its accumulator rows 128 r.. live in CTA r's TMEM. Per SM
+// and k-block this moves 32 KiB instead of 48 KiB, and the ring is 6 deep.
+//   full[s]   (even CTA only) : its own arrive.expect_tx of the pair's bytes +
+//                               the byte counts of both CTAs' loads
+//   empty[s]  (both CTAs)     : multicast commit from the even CTA's MMAs
+//   tfull[a]  (both CTAs)     : multicast commit after a tile's last k-block
+//   tempty[a] (even CTA only) : one arrival per epilogue warp of both CTAs
+// ============================================================================
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 columns of B
+constexpr int P_TILE_M = 256;
+
+struct PairSmemLayout {
+  static constexpr int kTiles = P_STAGES * (P_A_BYTES + P_B_BYTES);
+  static constexpr int kStaging = kTiles;
+  static constexpr int kBars = kStaging + EPI_WARPS * STAGE_TILE_BYTES;
+  static constexpr int kNumBars = 2 * P_STAGES + 4 + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kDynamicBytes = kTotal + 1024;
+};
+static_assert(PairSmemLayout::kDynamicBytes <= 232448, "shared memory budget (pair kernel)");
+
+__device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int lane) {
+  int ok = 0;
+  if (lane == 0) ok = mbar_wait_cluster(bar, parity, abort) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Bounded pause (used only when leaving after a timeout, so that copies the
+// CTA issued have landed before the pair is released).
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 < ns) {
+  }
+}
+
+template <bool A_MN, bool B_MN, class Epi>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmC, GemmGeom g, typename Epi::Params ep) {
+  if (Epi::skip(ep)) return;  // same value in both CTAs of the pair (one global word)
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + P_STAGES * P_A_BYTES;
+  uint8_t* staging = smem + PairSmemLayout::kStaging;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PairSmemLayout::kBars);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + P_STAGES;
+  uint64_t* tfull = bars + 2 * P_STAGES;
+  uint64_t* tempty = bars + 2 * P_STAGES + 2;
+  uint64_t* drain = bars + 2 * P_STAGES + 4;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + PairSmemLayout::kMisc);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + PairSmemLayout::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cluster = static_cast<int>(blockIdx.x >> 1);
+  const int nclusters = static_cast<int>(gridDim.x >> 1);
+  const int num_tiles = g.m_tiles * g.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_holder, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before anything signals them
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t armed = 0, armed_parity = 0;
+    bool ok = true;
+    for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+      int mb, nb;
+      tile_coords(g, t, mb, nb);
+      const int m0 = mb * P_TILE_M + static_cast<int>(rank) * 128;  // this CTA's A rows
+      const int nh = nb * BN + static_cast<int>(rank) * 128;         // this CTA's B columns
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort)) {
+          report_timeout(abort, g.flags);
+          ok = false;
+          break;
+        }
+        const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
+        const int k0 = kb * BK;
+        uint8_t* a_dst = sA + stage * P_A_BYTES;
+        uint8_t* b_dst = sB + stage * P_B_BYTES;
+        if (A_MN) {
+          tma_load_2d_pair(a_dst, &tmA, fbar, m0, k0);
+          tma_load_2d_pair(a_dst + MN_SLAB_BYTES, &tmA, fbar, m0 + 64, k0);
+        } else {
+          tma_load_2d_pair(a_dst, &tmA, fbar, k0, m0);
+        }
+        if (B_MN) {
+          tma_load_2d_pair(b_dst, &tmB, fbar, nh, k0);
+          tma_load_2d_pair(b_dst + MN_SLAB_BYTES, &tmB, fbar, nh + 64, k0);
+        } else {
+          tma_load_2d_pair(b_dst, &tmB, fbar, k0, nh);
+        }
+        armed |= 1u << stage;
+        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok || *abort) {
+      if (rank == 0)
+        for (int s = 0; s < P_STAGES; ++s)
+          if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u, 100000000ull);
+      pause_ns(200000);  // let copies this CTA issued land before the pair is released
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ---------------- MMA issuer (even CTA) ----------------
+    constexpr uint32_t idesc = idesc_bf16_f32(P_TILE_M, BN, A_MN, B_MN);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued = false;
+    for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+      if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
+        report_timeout(abort, g.flags);
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      for (int kb = 0; kb < g.k_blocks; ++kb) {
+        if (!mbar_wait_cluster(&full[stage], phase, abort)) {
+          report_timeout(abort, g.flags);
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t a_addr = smem_u32(sA + stage * P_A_BYTES);
+        const uint32_t b_addr = smem_u32(sB + stage * P_B_BYTES);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + k * 2048, MN_SLAB_BYTES, 1024)
+                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
+          const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + k * 2048, MN_SLAB_BYTES, 1024)
+                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
+          umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        }
+        issued = true;
+        umma_commit_pair(&empty[stage], 0x3);
+        if (++stage == P_STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      umma_commit_pair(&tfull[acc], 0x3);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (*abort && issued) {
+      umma_commit_pair(drain, 0x1);
+      mbar_wait_drain(drain, 0, 100000000ull);
+    }
+  } else if (warp >= EPI_WARP0) {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int e = warp - EPI_WARP0;
+    const int q = warp & 3;
+    const int half = e >> 2;
+    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, &tmC, lane, q * 32};
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    typename Epi::State st;
+    Epi::init(ep, st);
+    for (int t = cluster; t < num_tiles; t += nclusters) {
+      if (!warp_wait_cluster(&tfull[acc], acc_phase, abort, lane)) {
+        if (lane == 0) report_timeout(abort, g.flags);
+        break;
+      }
+      tc_fence_after_sync();
+      int mb, nb;
+      tile_coords(g, t, mb, nb);
+      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                             static_cast<uint32_t>(acc * BN + half * EPI_COLS);
+      Epi::tile(ep, st, ctx, mb * P_TILE_M + static_cast<int>(rank) * 128, nb * BN + half * EPI_COLS, taddr);
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before_sync();
+  __syncwarp();        // the cluster barrier below is warp-aligned
+  __syncthreads();
+  cluster_sync_all();  // neither CTA leaves while the other may still signal it
+  tc_fence_after_sync();
+  if (warp == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+}
+
 }  // namespace lce

@@ -72,8 +72,10 @@ struct DwParams {
   const DevStatus* st;   // gscale
 };
 
+// Logical GEMM shape D[M, N] = A[M, K] B[N, K]^T; the launcher picks the tiling.
 struct GemmGeomHost {
-  int m_tiles, n_tiles, k_blocks, m_fast;
+  long long M, N, K;
+  int m_fast;   // 1: consecutive tiles walk M first (they share the B tile)
 };
 
 // Kernel launches (return cudaGetLastError()).
@@ -96,10 +98,11 @@ cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, 
                           cudaStream_t s);
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
 
-// GEMM tile geometry (must match the kernels).
-constexpr int kTileM = 128;
-constexpr int kTileN = 256;
-constexpr int kTileK = 64;
+// GEMM tile geometry (must match the kernels): each CTA of a pair loads 128
+// rows of a K-major operand per box and 64 rows of an MN-major one.
+constexpr int kBoxRowsK = 128;
+constexpr int kBoxRowsMN = 64;
+constexpr int kTileN = 256;   // vocabulary tile of the logits GEMM (partials: two per tile)
 int gemm_smem_bytes();
 
 }  // namespace lce

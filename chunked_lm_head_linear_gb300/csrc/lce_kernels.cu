@@ -384,25 +384,28 @@ __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ los
 // ----------------------------------------------------------------------------
 // Launch wrappers
 // ----------------------------------------------------------------------------
-int gemm_smem_bytes() { return SmemLayout::kDynamicBytes; }
+int gemm_smem_bytes() { return PairSmemLayout::kDynamicBytes; }
 
 template <bool A_MN, bool B_MN, class Epi>
 static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                                const GemmGeomHost& gh, const typename Epi::Params& ep, int* flags, int num_sms,
                                cudaStream_t s) {
-  auto kern = gemm_kernel<A_MN, B_MN, Epi>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SmemLayout::kDynamicBytes);
+  // CTA pairs: 256 x 256 output tiles, one cluster of two CTAs per TPC.
+  auto kern = gemm_pair_kernel<A_MN, B_MN, Epi>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmemLayout::kDynamicBytes);
   if (e != cudaSuccess) return e;
   GemmGeom g;
-  g.m_tiles = gh.m_tiles;
-  g.n_tiles = gh.n_tiles;
-  g.k_blocks = gh.k_blocks;
+  g.m_tiles = static_cast<int>((gh.M + P_TILE_M - 1) / P_TILE_M);
+  g.n_tiles = static_cast<int>((gh.N + BN - 1) / BN);
+  g.k_blocks = static_cast<int>((gh.K + BK - 1) / BK);
   g.m_fast = gh.m_fast;
   g.flags = flags;
-  const int tiles = gh.m_tiles * gh.n_tiles;
+  const long long tiles = static_cast<long long>(g.m_tiles) * g.n_tiles;
   if (tiles <= 0) return cudaSuccess;
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  kern<<<grid, NUM_THREADS, SmemLayout::kDynamicBytes, s>>>(a, b, c, g, ep);
+  const int max_clusters = num_sms / 2;
+  const int clusters = tiles < max_clusters ? static_cast<int>(tiles) : max_clusters;
+  kern<<<2 * clusters, NUM_THREADS, PairSmemLayout::kDynamicBytes, s>>>(a, b, c, g, ep);
   return cudaGetLastError();
 }
 
