@@ -180,15 +180,15 @@ enum Kind : int {
   K_LOGITS_STATS = 1,   // FWD_STATS and FWD_STATS_P
   K_COMBINE = 2,
   K_LOGITS_GRAD = 3,    // unconditional FWD_GRAD (lce_backward)
-  K_GEMM_DH = 4,
-  K_GEMM_DW = 5,
+  K_GEMM_BWD = 4,       // dH and dW GEMMs of a chunk (one launch)
+  K_RESERVED = 5,
   K_FINALIZE = 6,
   K_OTHER = 7,          // memsets and the guard-conditional FWD_GRAD (work counted as 0)
   K_LOGITS_REF = 8,
   K_HSCALE = 9,
 };
 const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",  "logits_stats", "combine",    "logits_grad",
-                                                  "gemm_dH",  "gemm_dW",      "finalize",   "other",
+                                                  "gemm_dH_dW", "reserved",   "finalize",   "other",
                                                   "logits_ref", "hscale"};
 
 struct ProfRecord {
@@ -263,8 +263,7 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
     LCE_TRY(make_map(&mC, a.P, rows, c.V, c.L.ldp, kStoreRows));
   else
     mC = mB;  // this epilogue stores nothing
-  const int n_tiles = a.mode == lce::FWD_REF ? 1 : static_cast<int>(c.L.T);
-  lce::GemmGeomHost g{rows, a.mode == lce::FWD_REF ? lce::kTileN : c.V, c.d, 1};
+  const int64_t ncols = a.mode == lce::FWD_REF ? lce::kTileN : c.V;  // FWD_REF: the first vocabulary tile only
   lce::FwdParams p;
   std::memset(&p, 0, sizeof p);
   p.mode = a.mode;
@@ -282,13 +281,12 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   p.flags = &c.st->flags;
   p.guard = a.guard;
   p.only_if = a.only_if;
-  const double flops =
-      2.0 * static_cast<double>(rows) * static_cast<double>(n_tiles == 1 ? lce::kTileN : c.V) * static_cast<double>(c.d);
+  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(ncols) * static_cast<double>(c.d);
   int kind = K_LOGITS_STATS;
   if (a.mode == lce::FWD_REF) kind = K_LOGITS_REF;
   if (a.mode == lce::FWD_GRAD) kind = a.only_if ? K_OTHER : K_LOGITS_GRAD;
   return timed(c.s, kind, a.only_if ? 0.0 : flops,
-               [&] { return cuda_rc(lce::launch_fwd_gemm(mA, mB, mC, g, p, c.dev.num_sms, c.s)); });
+               [&] { return cuda_rc(lce::launch_logits(mA, mB, mC, rows, ncols, c.d, p, c.dev.num_sms, c.s)); });
 }
 
 int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* loss_i) {
@@ -305,18 +303,17 @@ int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* lo
 }
 
 // dH_c = (g/n) [rowscale] (G W) and dW (+)= (g/n) G^T B, with G [rows, V] in
-// the chunk's tile buffer and B = H_c or Ht.
+// the chunk's tile buffer and B = H_c or Ht: one launch for both GEMMs.
 int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, uint16_t* dH, float* dW,
           bool accumulate) {
   const uint16_t* P = reinterpret_cast<const uint16_t*>(c.ws + c.L.P);
-  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
-
-  // dH_c: A = G_c [rows, V] K-major, B = W [V, d] read N-major.
-  CUtensorMap mG, mW, mdH;
-  LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kBoxRowsK));
-  LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, lce::kBoxRowsMN));
-  LCE_TRY(make_map(&mdH, dH + c0 * c.d, rows, c.d, c.d, kStoreRows));
-  lce::GemmGeomHost gh{rows, c.d, c.V, 0};
+  CUtensorMap mG, mW, mdH, mGt, mB, mdW;
+  LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kBoxRowsK));      // dH: A, K-major
+  LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, lce::kBoxRowsMN));        // dH: B, N-major
+  LCE_TRY(make_map(&mdH, dH + c0 * c.d, rows, c.d, c.d, kStoreRows));  // dH store
+  LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, lce::kBoxRowsMN));    // dW: A, M-major
+  LCE_TRY(make_map(&mB, B, rows, c.d, c.d, lce::kBoxRowsMN));          // dW: B, N-major
+  LCE_TRY(make_map_t(&mdW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, c.V, c.d, c.d, 32u, kStoreRows));
   lce::DhParams dp;
   dp.rows = static_cast<int>(rows);
   dp.N = static_cast<int>(c.d);
@@ -324,15 +321,6 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   dp.ld = c.d;
   dp.rowscale = rowscale;
   dp.st = c.st;
-  LCE_TRY(timed(c.s, K_GEMM_DH, flops,
-                [&] { return cuda_rc(lce::launch_dh_gemm(mG, mW, mdH, gh, dp, &c.st->flags, c.dev.num_sms, c.s)); }));
-
-  // dW: A = G_c^T (G_c read M-major), B = [rows, d] read N-major.
-  CUtensorMap mGt, mB, mdW;
-  LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, lce::kBoxRowsMN));
-  LCE_TRY(make_map(&mB, B, rows, c.d, c.d, lce::kBoxRowsMN));
-  LCE_TRY(make_map_t(&mdW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, c.V, c.d, c.d, 32u, kStoreRows));
-  lce::GemmGeomHost gw{c.V, c.d, rows, 0};
   lce::DwParams wp;
   wp.rows = static_cast<int>(c.V);
   wp.N = static_cast<int>(c.d);
@@ -340,8 +328,11 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   wp.ld = c.d;
   wp.accumulate = accumulate ? 1 : 0;
   wp.st = c.st;
-  return timed(c.s, K_GEMM_DW, flops,
-               [&] { return cuda_rc(lce::launch_dw_gemm(mGt, mB, mdW, gw, wp, &c.st->flags, c.dev.num_sms, c.s)); });
+  const double flops = 4.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
+  return timed(c.s, K_GEMM_BWD, flops, [&] {
+    return cuda_rc(lce::launch_backward(mG, mW, mdH, mGt, mB, mdW, rows, c.V, c.d, dp, wp, &c.st->flags,
+                                        c.dev.num_sms, c.s));
+  });
 }
 
 // Backward of one chunk from a known lse: recompute the logits into the

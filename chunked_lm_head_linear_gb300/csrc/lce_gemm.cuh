@@ -8,17 +8,20 @@
 // ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation", section 3.1.4:
 // the logits chunk, and the backward's d_input / d_weight.)
 //
-// One CTA per SM, 384 threads:
-//   warp 0      TMA producer (one thread): A/B k-blocks into a STAGES-deep ring
-//   warp 1      MMA issuer (one thread): tcgen05.mma 128x256x16, fp32 in TMEM
+// The kernel runs on clusters of two CTAs (one TPC each) and computes 256 x 256
+// output tiles with tcgen05.mma.cta_group::2. Each CTA has 384 threads:
+//   warp 0      TMA producer (one thread): its CTA's half of the A/B k-blocks
+//   warp 1      MMA issuer (one thread, even CTA of the pair)
 //   warp 2      TMEM allocator (512 columns = two 128x256 fp32 accumulators)
 //   warps 4-11  epilogue: warp w reads TMEM lanes 32*(w%4).. (the hardware
 //               lane quarter of its sub-partition) and columns
-//               128*((w-4)/4).. of the tile, does the per-tile arithmetic and
-//               writes results through its own 4 KiB shared-memory staging
-//               tile with TMA stores (or TMA reduce-adds).
+//               128*((w-4)/4).. of its CTA's 128 rows, does the per-tile
+//               arithmetic and writes results through its own 4 KiB
+//               shared-memory staging tile with TMA stores (or reduce-adds).
 // The two accumulators alternate so the epilogue of tile t overlaps the main
-// loop of tile t+1. Tiles are assigned statically: tile = blockIdx.x + i*grid.
+// loop of tile t+1. What is multiplied, how operands are loaded and what the
+// epilogue does come from a problem type (see lce_kernels.cu): one GEMM, or
+// the dH and dW GEMMs of the backward in one launch.
 #pragma once
 
 #include "lce_internal.h"
@@ -29,9 +32,6 @@ namespace lce {
 constexpr int BM = 128;             // rows of an output tile (TMEM lanes)
 constexpr int BN = 256;             // columns of an output tile (TMEM columns)
 constexpr int BK = 64;              // k-block: 64 bf16 = one 128-byte swizzle row
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;   // 16 KiB
-constexpr int B_STAGE_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int MN_SLAB_BYTES = 64 * BK * 2;   // one 64-wide MN slab of a k-block: 8 KiB
 constexpr int EPI_WARP0 = 4;
 constexpr int EPI_WARPS = 8;
@@ -40,22 +40,40 @@ constexpr int NUM_THREADS = 32 * (EPI_WARP0 + EPI_WARPS);
 constexpr int STAGE_TILE_BYTES = 4096;       // 32 rows x 128 bytes, 128-byte swizzled
 constexpr int TMEM_COLS = 2 * BN;
 
-struct GemmGeom {
-  int m_tiles, n_tiles, k_blocks;
-  int m_fast;        // 1: consecutive tiles walk M first (share the B tile)
-  int* flags;        // device status word (timeout is reported here)
-};
+// ============================================================================
+// The CTA-pair kernel: tcgen05.mma.cta_group::2, 256 x 256 output tile per
+// pair. CTA rank r of the pair loads rows [128 r, 128 r + 128) of the A tile
+// and columns [128 r, 128 r + 128) of the B tile into its own shared memory;
+// the even CTA's MMA thread multiplies across both, and accumulator rows
+// 128 r.. live in CTA r's TMEM. Per SM and 64-deep k-block this moves 32 KiB,
+// and the ring is 6 deep.
+//   full[s]   (even CTA only) : its own arrive.expect_tx of the pair's bytes +
+//                               the byte counts of both CTAs' loads
+//   empty[s]  (both CTAs)     : multicast commit from the even CTA's MMAs
+//   tfull[a]  (both CTAs)     : multicast commit after a tile's last k-block
+//   tempty[a] (even CTA only) : one arrival per epilogue warp of both CTAs
+// ============================================================================
+constexpr int P_STAGES = 6;
+constexpr int P_A_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 rows of A
+constexpr int P_B_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 columns of B
+constexpr int P_TILE_M = 256;
 
-struct SmemLayout {
-  static constexpr int kTiles = STAGES * (A_STAGE_BYTES + B_STAGE_BYTES);
-  static constexpr int kStaging = kTiles;                          // EPI_WARPS staging tiles
+struct PairSmemLayout {
+  static constexpr int kTiles = P_STAGES * (P_A_BYTES + P_B_BYTES);
+  static constexpr int kStaging = kTiles;
   static constexpr int kBars = kStaging + EPI_WARPS * STAGE_TILE_BYTES;
-  static constexpr int kNumBars = 2 * STAGES + 4 + 1;   // full, empty, tmem_full[2], tmem_empty[2], drain
-  static constexpr int kMisc = kBars + kNumBars * 8;    // tmem holder + abort flag
+  static constexpr int kNumBars = 2 * P_STAGES + 4 + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
-  static constexpr int kDynamicBytes = kTotal + 1024;   // slack for 1 KiB alignment
+  static constexpr int kDynamicBytes = kTotal + 1024;
 };
-static_assert(SmemLayout::kDynamicBytes <= 232448, "shared memory budget");
+static_assert(PairSmemLayout::kDynamicBytes <= 232448, "shared memory budget (pair kernel)");
+
+// A tile of work: which GEMM of the problem (kind), its 256-row block, its
+// 256-column block and its number of k-blocks.
+struct TileJob {
+  int kind, mb, nb, k_blocks;
+};
 
 // What an epilogue warp needs besides its tile: its staging tile, the store
 // map and where its 32 rows start.
@@ -90,244 +108,21 @@ __device__ __forceinline__ void stage_release(const EpiCtx& c, int x, int y, boo
   }
 }
 
-__device__ __forceinline__ void tile_coords(const GemmGeom& g, int t, int& m_blk, int& n_blk) {
-  if (g.m_fast) {
-    m_blk = t % g.m_tiles;
-    n_blk = t / g.m_tiles;
-  } else {
-    n_blk = t % g.n_tiles;
-    m_blk = t / g.n_tiles;
-  }
-}
-
-// Broadcast a lane-0 wait result to the warp so every lane takes the same path
-// (the epilogue's tcgen05.ld instructions are warp-collective).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort, int lane) {
-  int ok = 0;
-  if (lane == 0) ok = mbar_wait(bar, parity, abort) ? 1 : 0;
-  return __shfl_sync(0xffffffffu, ok, 0) != 0;
-}
-
 __device__ __forceinline__ void report_timeout(volatile int* abort, int* flags) {
   *abort = 1;
   atomicOr(flags, kFlagTimeout);
 }
 
-template <bool A_MN, bool B_MN, class Epi>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, GemmGeom g, typename Epi::Params ep) {
-  if (Epi::skip(ep)) return;  // conditional launch whose condition is false: no work at all
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
-
-  uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
-  uint8_t* staging = smem + SmemLayout::kStaging;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SmemLayout::kBars);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + STAGES;
-  uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
-  uint64_t* drain = bars + 2 * STAGES + 4;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + SmemLayout::kMisc);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + SmemLayout::kMisc + 4);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int num_tiles = g.m_tiles * g.n_tiles;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 32 * EPI_WARPS);
-    }
-    mbar_init(drain, 1);
-    *abort = 0;
-    fence_mbarrier_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
-  }
-  if (warp == 2) {
-    tmem_alloc(tmem_holder, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_holder;
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t armed = 0;             // bit s: stage s has a load in flight we armed
-    uint32_t armed_parity = 0;      // bit s: parity of that load's phase
-    bool ok = true;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      int mb, nb;
-      tile_coords(g, t, mb, nb);
-      const int m0 = mb * BM, n0 = nb * BN;
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort)) {
-          report_timeout(abort, g.flags);
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(&full[stage], A_STAGE_BYTES + B_STAGE_BYTES);
-        const int k0 = kb * BK;
-        uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
-        uint8_t* b_dst = sB + stage * B_STAGE_BYTES;
-        if (A_MN) {
-#pragma unroll
-          for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * MN_SLAB_BYTES, &tmA, &full[stage], m0 + 64 * j, k0);
-        } else {
-          tma_load_2d(a_dst, &tmA, &full[stage], k0, m0);
-        }
-        if (B_MN) {
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * MN_SLAB_BYTES, &tmB, &full[stage], n0 + 64 * j, k0);
-        } else {
-          tma_load_2d(b_dst, &tmB, &full[stage], k0, n0);
-        }
-        armed |= 1u << stage;
-        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    if (!ok || *abort) {
-      // Leave no copy in flight: wait (briefly) for every load this thread armed.
-      for (int s = 0; s < STAGES; ++s)
-        if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u, 100000000ull);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    bool issued = false;
-    for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort)) {
-        report_timeout(abort, g.flags);
-        break;
-      }
-      tc_fence_after_sync();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
-        if (!mbar_wait(&full[stage], phase, abort)) {
-          report_timeout(abort, g.flags);
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t a_addr = smem_u32(sA + stage * A_STAGE_BYTES);
-        const uint32_t b_addr = smem_u32(sB + stage * B_STAGE_BYTES);
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          // K-major: the next 16 elements are 32 bytes further along the row.
-          // MN-major: the next 16 K rows are 16 * 128 bytes further.
-          const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + k * 2048, MN_SLAB_BYTES, 1024)
-                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + k * 2048, MN_SLAB_BYTES, 1024)
-                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-          umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-        }
-        issued = true;
-        umma_commit(&empty[stage]);
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (!ok) break;
-      umma_commit(&tfull[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    if (*abort && issued) {
-      // Make sure no MMA still writes TMEM before it is released.
-      umma_commit(drain);
-      mbar_wait_drain(drain, 0, 100000000ull);
-    }
-  } else if (warp >= EPI_WARP0) {
-    // ---------------- epilogue ----------------
-    const int e = warp - EPI_WARP0;   // 0 .. EPI_WARPS-1
-    const int q = warp & 3;           // TMEM lane quarter this warp may access
-    const int half = e >> 2;          // which 128 columns of the tile
-    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, &tmC, lane, q * 32};
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    typename Epi::State st;
-    Epi::init(ep, st);
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
-      if (!warp_wait(&tfull[acc], acc_phase, abort, lane)) {
-        if (lane == 0) report_timeout(abort, g.flags);
-        break;
-      }
-      tc_fence_after_sync();
-      int mb, nb;
-      tile_coords(g, t, mb, nb);
-      const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN + half * EPI_COLS);
-      Epi::tile(ep, st, ctx, mb * BM, nb * BN + half * EPI_COLS, taddr);
-      tc_fence_before_sync();
-      mbar_arrive(&tempty[acc]);
-      if (++acc == 2) {
-        acc = 0;
-        acc_phase ^= 1u;
-      }
-    }
-    if (lane == 0) bulk_wait_all();   // every store of this warp has landed
-    __syncwarp();
-  }
-
-  tc_fence_before_sync();
-  __syncthreads();
-  tc_fence_after_sync();
-  if (warp == 2) tmem_dealloc(tmem_base, TMEM_COLS);
+// Shared-memory descriptors of one 16-deep K step (k = 0..3 within a 64-wide
+// k-block) of a 128-row (or 128-column) operand half in 128-byte swizzle:
+// K-major: the next 16 elements are 32 bytes further along each row;
+// MN-major: two 64-wide slabs 8 KiB apart, the next 16 K rows 2 KiB further.
+__device__ __forceinline__ uint64_t desc_k_major(uint32_t addr, int k) {
+  return smem_desc_sw128(addr + k * 32, 16, 1024);
 }
-
-// ============================================================================
-// CTA-pair variant: tcgen05.mma.cta_group::2, 256 x 256 output tile per pair.
-// Launched with clusters of two CTAs (one TPC). CTA rank r of the pair loads
-// rows [128 r, 128 r + 128) of the A tile and columns [128 r, 128 r + 128) of
-// the B tile into its own shared memory; the even CTA's MMA thread multiplies
-// across both, and its accumulator rows 128 r.. live in CTA r's TMEM. Per SM
-// and k-block this moves 32 KiB instead of 48 KiB, and the ring is 6 deep.
-//   full[s]   (even CTA only) : its own arrive.expect_tx of the pair's bytes +
-//                               the byte counts of both CTAs' loads
-//   empty[s]  (both CTAs)     : multicast commit from the even CTA's MMAs
-//   tfull[a]  (both CTAs)     : multicast commit after a tile's last k-block
-//   tempty[a] (even CTA only) : one arrival per epilogue warp of both CTAs
-// ============================================================================
-constexpr int P_STAGES = 6;
-constexpr int P_A_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 rows of A
-constexpr int P_B_BYTES = 128 * BK * 2;   // 16 KiB: this CTA's 128 columns of B
-constexpr int P_TILE_M = 256;
-
-struct PairSmemLayout {
-  static constexpr int kTiles = P_STAGES * (P_A_BYTES + P_B_BYTES);
-  static constexpr int kStaging = kTiles;
-  static constexpr int kBars = kStaging + EPI_WARPS * STAGE_TILE_BYTES;
-  static constexpr int kNumBars = 2 * P_STAGES + 4 + 1;
-  static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 16;
-  static constexpr int kDynamicBytes = kTotal + 1024;
-};
-static_assert(PairSmemLayout::kDynamicBytes <= 232448, "shared memory budget (pair kernel)");
+__device__ __forceinline__ uint64_t desc_mn_major(uint32_t addr, int k) {
+  return smem_desc_sw128(addr + k * 2048, MN_SLAB_BYTES, 1024);
+}
 
 __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort, int lane) {
   int ok = 0;
@@ -343,11 +138,20 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
   }
 }
 
-template <bool A_MN, bool B_MN, class Epi>
+// Problem interface (Prob):
+//   Params                      kernel parameters (tensor maps, shapes, epilogue params)
+//   State                       per-epilogue-thread constants
+//   skip(p)                     conditional launch: true = do nothing
+//   flags(p)                    device status word
+//   num_jobs(p, cluster, P)     number of tiles of this cluster (P clusters in the grid)
+//   job(p, cluster, P, j)       its j-th tile
+//   load(p, kind, a, b, bar, m0, n0, k0)  this CTA's half of the k-block (TMA, pair form)
+//   a_desc / b_desc(kind, addr, k), idesc(kind)   MMA descriptors
+//   init(p, st), epilogue(p, st, kind, ctx, m0, col0, taddr)
+template <class Prob>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                     const __grid_constant__ CUtensorMap tmC, GemmGeom g, typename Epi::Params ep) {
-  if (Epi::skip(ep)) return;  // same value in both CTAs of the pair (one global word)
+    gemm_pair_kernel(const __grid_constant__ typename Prob::Params p) {
+  if (Prob::skip(p)) return;  // same value in both CTAs of the pair (one global word)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -369,7 +173,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const uint32_t rank = cluster_ctarank();
   const int cluster = static_cast<int>(blockIdx.x >> 1);
   const int nclusters = static_cast<int>(gridDim.x >> 1);
-  const int num_tiles = g.m_tiles * g.n_tiles;
+  const int njobs = Prob::num_jobs(p, cluster, nclusters);
+  int* flags = Prob::flags(p);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < P_STAGES; ++s) {
@@ -383,8 +188,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     mbar_init(drain, 1);
     *abort = 0;
     fence_mbarrier_init();
-    tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_holder, TMEM_COLS);
@@ -402,34 +205,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int t = cluster; t < num_tiles && ok; t += nclusters) {
-      int mb, nb;
-      tile_coords(g, t, mb, nb);
-      const int m0 = mb * P_TILE_M + static_cast<int>(rank) * 128;  // this CTA's A rows
-      const int nh = nb * BN + static_cast<int>(rank) * 128;         // this CTA's B columns
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
+    for (int j = 0; j < njobs && ok; ++j) {
+      const TileJob tj = Prob::job(p, cluster, nclusters, j);
+      const int m0 = tj.mb * P_TILE_M + static_cast<int>(rank) * 128;  // this CTA's A rows
+      const int nh = tj.nb * BN + static_cast<int>(rank) * 128;         // this CTA's B columns
+      for (int kb = 0; kb < tj.k_blocks; ++kb) {
         if (!mbar_wait_cluster(&empty[stage], phase ^ 1u, abort)) {
-          report_timeout(abort, g.flags);
+          report_timeout(abort, flags);
           ok = false;
           break;
         }
         const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
         if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
-        const int k0 = kb * BK;
-        uint8_t* a_dst = sA + stage * P_A_BYTES;
-        uint8_t* b_dst = sB + stage * P_B_BYTES;
-        if (A_MN) {
-          tma_load_2d_pair(a_dst, &tmA, fbar, m0, k0);
-          tma_load_2d_pair(a_dst + MN_SLAB_BYTES, &tmA, fbar, m0 + 64, k0);
-        } else {
-          tma_load_2d_pair(a_dst, &tmA, fbar, k0, m0);
-        }
-        if (B_MN) {
-          tma_load_2d_pair(b_dst, &tmB, fbar, nh, k0);
-          tma_load_2d_pair(b_dst + MN_SLAB_BYTES, &tmB, fbar, nh + 64, k0);
-        } else {
-          tma_load_2d_pair(b_dst, &tmB, fbar, k0, nh);
-        }
+        Prob::load(p, tj.kind, sA + stage * P_A_BYTES, sB + stage * P_B_BYTES, fbar, m0, nh, kb * BK);
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == P_STAGES) {
@@ -446,23 +234,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1 && lane == 0 && rank == 0) {
     // ---------------- MMA issuer (even CTA) ----------------
-    constexpr uint32_t idesc = idesc_bf16_f32(P_TILE_M, BN, A_MN, B_MN);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued = false;
-    for (int t = cluster; t < num_tiles && ok; t += nclusters) {
+    for (int j = 0; j < njobs && ok; ++j) {
+      const TileJob tj = Prob::job(p, cluster, nclusters, j);
+      const uint32_t idesc = Prob::idesc(tj.kind);
       if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
-        report_timeout(abort, g.flags);
+        report_timeout(abort, flags);
         break;
       }
       tc_fence_after_sync();
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      for (int kb = 0; kb < g.k_blocks; ++kb) {
+      for (int kb = 0; kb < tj.k_blocks; ++kb) {
         if (!mbar_wait_cluster(&full[stage], phase, abort)) {
-          report_timeout(abort, g.flags);
+          report_timeout(abort, flags);
           ok = false;
           break;
         }
@@ -470,13 +259,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         const uint32_t a_addr = smem_u32(sA + stage * P_A_BYTES);
         const uint32_t b_addr = smem_u32(sB + stage * P_B_BYTES);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = A_MN ? smem_desc_sw128(a_addr + k * 2048, MN_SLAB_BYTES, 1024)
-                                   : smem_desc_sw128(a_addr + k * 32, 16, 1024);
-          const uint64_t bd = B_MN ? smem_desc_sw128(b_addr + k * 2048, MN_SLAB_BYTES, 1024)
-                                   : smem_desc_sw128(b_addr + k * 32, 16, 1024);
-          umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < BK / 16; ++k)
+          umma_bf16_pair(d_tmem, Prob::a_desc(tj.kind, a_addr, k), Prob::b_desc(tj.kind, b_addr, k), idesc,
+                         (kb | k) != 0 ? 1u : 0u);
         issued = true;
         umma_commit_pair(&empty[stage], 0x3);
         if (++stage == P_STAGES) {
@@ -500,22 +285,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int e = warp - EPI_WARP0;
     const int q = warp & 3;
     const int half = e >> 2;
-    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, &tmC, lane, q * 32};
+    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, nullptr, lane, q * 32};
     int acc = 0;
     uint32_t acc_phase = 0;
-    typename Epi::State st;
-    Epi::init(ep, st);
-    for (int t = cluster; t < num_tiles; t += nclusters) {
+    typename Prob::State st;
+    Prob::init(p, st);
+    for (int j = 0; j < njobs; ++j) {
       if (!warp_wait_cluster(&tfull[acc], acc_phase, abort, lane)) {
-        if (lane == 0) report_timeout(abort, g.flags);
+        if (lane == 0) report_timeout(abort, flags);
         break;
       }
       tc_fence_after_sync();
-      int mb, nb;
-      tile_coords(g, t, mb, nb);
+      const TileJob tj = Prob::job(p, cluster, nclusters, j);
       const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                              static_cast<uint32_t>(acc * BN + half * EPI_COLS);
-      Epi::tile(ep, st, ctx, mb * P_TILE_M + static_cast<int>(rank) * 128, nb * BN + half * EPI_COLS, taddr);
+      Prob::epilogue(p, st, tj.kind, ctx, tj.mb * P_TILE_M + static_cast<int>(rank) * 128,
+                     tj.nb * BN + half * EPI_COLS, taddr);
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote(mapa_shared(smem_u32(&tempty[acc]), 0));

@@ -72,23 +72,21 @@ struct DwParams {
   const DevStatus* st;   // gscale
 };
 
-// Logical GEMM shape D[M, N] = A[M, K] B[N, K]^T; the launcher picks the tiling.
-struct GemmGeomHost {
-  long long M, N, K;
-  int m_fast;   // 1: consecutive tiles walk M first (they share the B tile)
-};
-
 // Kernel launches (return cudaGetLastError()).
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
                            long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
                            cudaStream_t s);
-// a, b: operand tensor maps; c: the epilogue's TMA store map (any valid map if unused).
-cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                            const FwdParams& p, int num_sms, cudaStream_t s);
-cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                           const DhParams& p, int* flags, int num_sms, cudaStream_t s);
-cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                           const DwParams& p, int* flags, int num_sms, cudaStream_t s);
+// Logits GEMM of a chunk: z [M, N] = A [M, K] B [N, K]^T with the FwdEpi
+// epilogue; a, b: K-major operand maps, c: the epilogue's store map (any valid
+// map if the mode stores nothing).
+cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, long long M, long long N,
+                          long long K, const FwdParams& ep, int num_sms, cudaStream_t s);
+// Backward GEMMs of a chunk in one launch: dH_c = G W (ah: G K-major, bh: W
+// N-major, ch: dH store) and dW (+)= G^T B (aw: G M-major, bw: B N-major, cw:
+// dW store / reduce-add).
+cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
+                            const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
+                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s);
 cudaError_t launch_combine(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
@@ -103,6 +101,5 @@ cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* s
 constexpr int kBoxRowsK = 128;
 constexpr int kBoxRowsMN = 64;
 constexpr int kTileN = 256;   // vocabulary tile of the logits GEMM (partials: two per tile)
-int gemm_smem_bytes();
 
 }  // namespace lce

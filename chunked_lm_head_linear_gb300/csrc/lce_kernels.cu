@@ -384,44 +384,203 @@ __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ los
 // ----------------------------------------------------------------------------
 // Launch wrappers
 // ----------------------------------------------------------------------------
-int gemm_smem_bytes() { return PairSmemLayout::kDynamicBytes; }
 
-template <bool A_MN, bool B_MN, class Epi>
-static cudaError_t launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
-                               const GemmGeomHost& gh, const typename Epi::Params& ep, int* flags, int num_sms,
-                               cudaStream_t s) {
-  // CTA pairs: 256 x 256 output tiles, one cluster of two CTAs per TPC.
-  auto kern = gemm_pair_kernel<A_MN, B_MN, Epi>;
+// ----------------------------------------------------------------------------
+// Problems for the pair kernel
+// ----------------------------------------------------------------------------
+enum : int { KIND_LOGITS = 0, KIND_DH = 1, KIND_DW = 2 };
+
+// This CTA's half of a k-block: 128 rows of a K-major operand (one box), or
+// 128 columns of an MN-major operand (two 64-wide boxes).
+__device__ __forceinline__ void load_k_major(uint8_t* dst, const CUtensorMap* m, uint32_t bar, int row0, int k0) {
+  tma_load_2d_pair(dst, m, bar, k0, row0);
+}
+__device__ __forceinline__ void load_mn_major(uint8_t* dst, const CUtensorMap* m, uint32_t bar, int mn0, int k0) {
+  tma_load_2d_pair(dst, m, bar, mn0, k0);
+  tma_load_2d_pair(dst + MN_SLAB_BYTES, m, bar, mn0 + 64, k0);
+}
+
+// Logits of a chunk: z = H_c W^T (both operands K-major) with the FwdEpi
+// epilogue. Tiles walk M first, so the pairs running at once share W tiles.
+struct LogitsProb {
+  struct Params {
+    CUtensorMap a, b, c;
+    int m_tiles, n_tiles, k_blocks;
+    int* flags;
+    FwdParams ep;
+  };
+  using State = FwdEpi::State;
+  static __device__ __forceinline__ bool skip(const Params& p) { return FwdEpi::skip(p.ep); }
+  static __device__ __forceinline__ int* flags(const Params& p) { return p.flags; }
+  static __device__ __forceinline__ int num_jobs(const Params& p, int c, int P) {
+    const int tiles = p.m_tiles * p.n_tiles;
+    return c < tiles ? (tiles - 1 - c) / P + 1 : 0;
+  }
+  static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
+    const int t = c + j * P;
+    return TileJob{KIND_LOGITS, t % p.m_tiles, t / p.m_tiles, p.k_blocks};
+  }
+  static __device__ __forceinline__ void load(const Params& p, int, uint8_t* a, uint8_t* b, uint32_t bar, int m0,
+                                              int n0, int k0) {
+    load_k_major(a, &p.a, bar, m0, k0);
+    load_k_major(b, &p.b, bar, n0, k0);
+  }
+  static __device__ __forceinline__ uint64_t a_desc(int, uint32_t addr, int k) { return desc_k_major(addr, k); }
+  static __device__ __forceinline__ uint64_t b_desc(int, uint32_t addr, int k) { return desc_k_major(addr, k); }
+  static __device__ __forceinline__ uint32_t idesc(int) { return idesc_bf16_f32(P_TILE_M, BN, false, false); }
+  static __device__ __forceinline__ void init(const Params& p, State& st) { FwdEpi::init(p.ep, st); }
+  static __device__ __forceinline__ void epilogue(const Params& p, State& st, int, EpiCtx ctx, int m0, int col0,
+                                                  uint32_t taddr) {
+    ctx.out = &p.c;
+    FwdEpi::tile(p.ep, st, ctx, m0, col0, taddr);
+  }
+};
+
+// The backward of a chunk in one launch: dH tiles (dH_c = G_c W: A = G_c
+// K-major, B = W N-major) and dW tiles (dW += G_c^T B: A = G_c read M-major,
+// B = Ht or H_c N-major). dH tiles are few and long (K = V), dW tiles many and
+// short (K = C); the static schedule deals the dH tiles round-robin, then
+// w_phase1 dW tiles round-robin to every cluster, then the remaining dW tiles
+// round-robin to the clusters that hold one dH tile fewer, so every cluster
+// ends with about the same number of k-blocks. Tiles walk N first, so the
+// pairs running at once share the A rows.
+struct BwdProb {
+  struct Params {
+    CUtensorMap ah, bh, ch, aw, bw, cw;
+    int h_m, h_n, h_k;   // dH: 256-row blocks of the chunk, 256-column blocks of d, k-blocks of V
+    int w_m, w_n, w_k;   // dW: 256-row blocks of V, 256-column blocks of d, k-blocks of the chunk
+    int w_phase1;        // dW tiles dealt round-robin to every cluster (a multiple of the cluster count)
+    int* flags;
+    DhParams h;
+    DwParams w;
+  };
+  struct State {
+    DhEpi::State h;
+    DwEpi::State w;
+  };
+  struct Sched {
+    int hcount, q1, li, nlight, count2;
+  };
+  static __device__ __forceinline__ Sched sched(const Params& p, int c, int P) {
+    Sched s;
+    const int nH = p.h_m * p.h_n, nW = p.w_m * p.w_n;
+    s.hcount = c < nH ? (nH - 1 - c) / P + 1 : 0;
+    const int r = nH % P;  // clusters c < r hold one dH tile more
+    s.q1 = p.w_phase1 / P;
+    s.nlight = r == 0 ? P : P - r;
+    s.li = r == 0 ? c : c - r;
+    const int rem = nW - p.w_phase1;
+    s.count2 = (s.li >= 0 && s.li < rem) ? (rem - 1 - s.li) / s.nlight + 1 : 0;
+    return s;
+  }
+  static __device__ __forceinline__ bool skip(const Params&) { return false; }
+  static __device__ __forceinline__ int* flags(const Params& p) { return p.flags; }
+  static __device__ __forceinline__ int num_jobs(const Params& p, int c, int P) {
+    const Sched s = sched(p, c, P);
+    return s.hcount + s.q1 + s.count2;
+  }
+  static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
+    const Sched s = sched(p, c, P);
+    if (j < s.hcount) {
+      const int t = c + j * P;
+      return TileJob{KIND_DH, t / p.h_n, t % p.h_n, p.h_k};
+    }
+    j -= s.hcount;
+    const int t = j < s.q1 ? c + j * P : p.w_phase1 + s.li + (j - s.q1) * s.nlight;
+    return TileJob{KIND_DW, t / p.w_n, t % p.w_n, p.w_k};
+  }
+  static __device__ __forceinline__ void load(const Params& p, int kind, uint8_t* a, uint8_t* b, uint32_t bar,
+                                              int m0, int n0, int k0) {
+    if (kind == KIND_DH) {
+      load_k_major(a, &p.ah, bar, m0, k0);
+      load_mn_major(b, &p.bh, bar, n0, k0);
+    } else {
+      load_mn_major(a, &p.aw, bar, m0, k0);
+      load_mn_major(b, &p.bw, bar, n0, k0);
+    }
+  }
+  static __device__ __forceinline__ uint64_t a_desc(int kind, uint32_t addr, int k) {
+    return kind == KIND_DH ? desc_k_major(addr, k) : desc_mn_major(addr, k);
+  }
+  static __device__ __forceinline__ uint64_t b_desc(int, uint32_t addr, int k) { return desc_mn_major(addr, k); }
+  static __device__ __forceinline__ uint32_t idesc(int kind) {
+    return kind == KIND_DH ? idesc_bf16_f32(P_TILE_M, BN, false, true) : idesc_bf16_f32(P_TILE_M, BN, true, true);
+  }
+  static __device__ __forceinline__ void init(const Params& p, State& st) {
+    DhEpi::init(p.h, st.h);
+    DwEpi::init(p.w, st.w);
+  }
+  static __device__ __forceinline__ void epilogue(const Params& p, State& st, int kind, EpiCtx ctx, int m0, int col0,
+                                                  uint32_t taddr) {
+    if (kind == KIND_DH) {
+      ctx.out = &p.ch;
+      DhEpi::tile(p.h, st.h, ctx, m0, col0, taddr);
+    } else {
+      ctx.out = &p.cw;
+      DwEpi::tile(p.w, st.w, ctx, m0, col0, taddr);
+    }
+  }
+};
+
+template <class Prob>
+static cudaError_t launch_pair(const typename Prob::Params& p, int clusters, cudaStream_t s) {
+  if (clusters <= 0) return cudaSuccess;
+  auto kern = gemm_pair_kernel<Prob>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmemLayout::kDynamicBytes);
   if (e != cudaSuccess) return e;
-  GemmGeom g;
-  g.m_tiles = static_cast<int>((gh.M + P_TILE_M - 1) / P_TILE_M);
-  g.n_tiles = static_cast<int>((gh.N + BN - 1) / BN);
-  g.k_blocks = static_cast<int>((gh.K + BK - 1) / BK);
-  g.m_fast = gh.m_fast;
-  g.flags = flags;
-  const long long tiles = static_cast<long long>(g.m_tiles) * g.n_tiles;
-  if (tiles <= 0) return cudaSuccess;
-  const int max_clusters = num_sms / 2;
-  const int clusters = tiles < max_clusters ? static_cast<int>(tiles) : max_clusters;
-  kern<<<2 * clusters, NUM_THREADS, PairSmemLayout::kDynamicBytes, s>>>(a, b, c, g, ep);
+  kern<<<2 * clusters, NUM_THREADS, PairSmemLayout::kDynamicBytes, s>>>(p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_fwd_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                            const FwdParams& p, int num_sms, cudaStream_t s) {
-  return launch_gemm<false, false, FwdEpi>(a, b, c, g, p, p.flags, num_sms, s);
+static int ceil_div_i(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
+
+cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, long long M, long long N,
+                          long long K, const FwdParams& ep, int num_sms, cudaStream_t s) {
+  LogitsProb::Params p;
+  p.a = a;
+  p.b = b;
+  p.c = c;
+  p.m_tiles = ceil_div_i(M, P_TILE_M);
+  p.n_tiles = ceil_div_i(N, BN);
+  p.k_blocks = ceil_div_i(K, BK);
+  p.flags = ep.flags;
+  p.ep = ep;
+  const long long tiles = static_cast<long long>(p.m_tiles) * p.n_tiles;
+  const int clusters = static_cast<int>(tiles < num_sms / 2 ? tiles : num_sms / 2);
+  return launch_pair<LogitsProb>(p, clusters, s);
 }
 
-cudaError_t launch_dh_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                           const DhParams& p, int* flags, int num_sms, cudaStream_t s) {
-  return launch_gemm<false, true, DhEpi>(a, b, c, g, p, flags, num_sms, s);
-}
-
-cudaError_t launch_dw_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const GemmGeomHost& g,
-                           const DwParams& p, int* flags, int num_sms, cudaStream_t s) {
-  return launch_gemm<true, true, DwEpi>(a, b, c, g, p, flags, num_sms, s);
+cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
+                            const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
+                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s) {
+  BwdProb::Params p;
+  p.ah = ah;
+  p.bh = bh;
+  p.ch = ch;
+  p.aw = aw;
+  p.bw = bw;
+  p.cw = cw;
+  p.h_m = ceil_div_i(rows, P_TILE_M);
+  p.h_n = ceil_div_i(d, BN);
+  p.h_k = ceil_div_i(V, BK);
+  p.w_m = ceil_div_i(V, P_TILE_M);
+  p.w_n = ceil_div_i(d, BN);
+  p.w_k = ceil_div_i(rows, BK);
+  p.flags = flags;
+  p.h = h;
+  p.w = w;
+  const long long nH = static_cast<long long>(p.h_m) * p.h_n, nW = static_cast<long long>(p.w_m) * p.w_n;
+  const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
+  if (P <= 0) return cudaSuccess;
+  // Balance: every cluster should end with ~(nH h_k + nW w_k) / P k-blocks.
+  const double target = (static_cast<double>(nH) * p.h_k + static_cast<double>(nW) * p.w_k) / P;
+  const long long hmax = (nH + P - 1) / P;
+  long long q1 = static_cast<long long>((target - static_cast<double>(hmax) * p.h_k) / p.w_k);
+  if (q1 < 0) q1 = 0;
+  if (q1 > nW / P) q1 = nW / P;
+  p.w_phase1 = static_cast<int>(q1 * P);
+  return launch_pair<BwdProb>(p, P, s);
 }
 
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
