@@ -439,10 +439,15 @@ struct LogitsProb {
 // The backward of a chunk in one launch: dH tiles (dH_c = G_c W: A = G_c
 // K-major, B = W N-major) and dW tiles (dW += G_c^T B: A = G_c read M-major,
 // B = Ht or H_c N-major). dH tiles are few and long (K = V), dW tiles many and
-// short (K = C); the static schedule deals the dH tiles round-robin, then
-// w_phase1 dW tiles round-robin to every cluster, then the remaining dW tiles
-// round-robin to the clusters that hold one dH tile fewer, so every cluster
-// ends with about the same number of k-blocks. Tiles walk N first, so the
+// short (K = C). The static schedule gives every cluster, in this order:
+//   1. w_phase1 / P dW tiles dealt round-robin to all clusters,
+//   2. its dH tiles, dealt round-robin,
+//   3. the remaining dW tiles, dealt round-robin to the clusters that hold
+//      one dH tile fewer,
+// so every cluster ends with about the same number of k-blocks, and the tiles
+// running at the same time are neighbours in their lists (they share operand
+// rows in L2): all clusters start phase 1 together, and the clusters of phase
+// 3 all enter it after the same number of dH tiles. Tiles walk N first, so the
 // pairs running at once share the A rows.
 struct BwdProb {
   struct Params {
@@ -481,12 +486,17 @@ struct BwdProb {
   }
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const Sched s = sched(p, c, P);
+    if (j < s.q1) {
+      const int t = c + j * P;
+      return TileJob{KIND_DW, t / p.w_n, t % p.w_n, p.w_k};
+    }
+    j -= s.q1;
     if (j < s.hcount) {
       const int t = c + j * P;
       return TileJob{KIND_DH, t / p.h_n, t % p.h_n, p.h_k};
     }
     j -= s.hcount;
-    const int t = j < s.q1 ? c + j * P : p.w_phase1 + s.li + (j - s.q1) * s.nlight;
+    const int t = p.w_phase1 + s.li + j * s.nlight;
     return TileJob{KIND_DW, t / p.w_n, t % p.w_n, p.w_k};
   }
   static __device__ __forceinline__ void load(const Params& p, int kind, uint8_t* a, uint8_t* b, uint32_t bar,
