@@ -115,7 +115,8 @@ int check_sizes(int64_t N, int64_t d, int64_t V, const lce_opts* o) {
   if (N > (int64_t{1} << 31) - 1 || V > (int64_t{1} << 31) - 1 || d > (int64_t{1} << 24)) return LCE_ERR_INVALID_ARG;
   if (o) {
     if (o->reduction != LCE_MEAN && o->reduction != LCE_SUM) return LCE_ERR_INVALID_ARG;
-    if (o->chunk_tokens < 0 || o->reserved != 0) return LCE_ERR_INVALID_ARG;
+    if (o->chunk_tokens < 0 || (o->reserved != 0 && o->reserved != LCE_TEST_FORCE_TIMEOUT))
+      return LCE_ERR_INVALID_ARG;
     if (o->accumulate_dW != 0 && o->accumulate_dW != 1) return LCE_ERR_INVALID_ARG;
   }
   return LCE_OK;
@@ -285,8 +286,10 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   int kind = K_LOGITS_STATS;
   if (a.mode == lce::FWD_REF) kind = K_LOGITS_REF;
   if (a.mode == lce::FWD_GRAD) kind = a.only_if ? K_OTHER : K_LOGITS_GRAD;
-  return timed(c.s, kind, a.only_if ? 0.0 : flops,
-               [&] { return cuda_rc(lce::launch_logits(mA, mB, mC, rows, ncols, c.d, p, c.dev.num_sms, c.s)); });
+  const int no_loads = (c.o.reserved == LCE_TEST_FORCE_TIMEOUT && a.mode == lce::FWD_STATS) ? 1 : 0;
+  return timed(c.s, kind, a.only_if ? 0.0 : flops, [&] {
+    return cuda_rc(lce::launch_logits(mA, mB, mC, rows, ncols, c.d, p, no_loads, c.dev.num_sms, c.s));
+  });
 }
 
 int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* loss_i) {
@@ -460,6 +463,19 @@ size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opt
   return make_layout(op, N, d, V, &o).total;
 }
 
+int64_t lce_auto_chunk(int64_t N, int64_t d, int64_t V, size_t budget_bytes, const lce_opts* opts) {
+  lce_opts o;
+  lce_opts_init(&o);
+  if (opts) o = *opts;
+  if (check_sizes(N, d, V, &o) != LCE_OK || N <= 0) return 0;
+  const int64_t cap = ((N + 255) / 256) * 256;
+  for (int64_t C = 4096 < cap ? 4096 : cap; C >= 256; C -= 256) {
+    o.chunk_tokens = C;
+    if (make_layout(LCE_OP_FWD_BWD, N, d, V, &o).total <= budget_bytes) return C;
+  }
+  return 0;
+}
+
 int lce_forward(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V, float* loss,
                 float* lse, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
   Call c;
@@ -482,6 +498,7 @@ int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int6
                  void* stream) {
   Call c;
   LCE_TRY(begin(&c, LCE_OP_BACKWARD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
+  if (c.o.reserved != 0) return LCE_ERR_INVALID_ARG;
   if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
   if (!aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
       (grad_loss && !aligned(grad_loss, 4)))
@@ -503,6 +520,7 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
                 size_t ws_bytes, void* stream) {
   Call c;
   LCE_TRY(begin(&c, LCE_OP_FWD_BWD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
+  if (c.o.reserved != 0) return LCE_ERR_INVALID_ARG;
   if (!loss || !dW || (N > 0 && !dH)) return LCE_ERR_INVALID_ARG;
   if (!aligned(loss, 4) || !aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
       (grad_loss && !aligned(grad_loss, 4)))

@@ -142,6 +142,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 //   Params                      kernel parameters (tensor maps, shapes, epilogue params)
 //   State                       per-epilogue-thread constants
 //   skip(p)                     conditional launch: true = do nothing
+//   no_loads(p)                 timeout test: the producer issues no loads
 //   flags(p)                    device status word
 //   num_jobs(p, cluster, P)     number of tiles of this cluster (P clusters in the grid)
 //   job(p, cluster, P, j)       its j-th tile
@@ -204,7 +205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     int stage = 0;
     uint32_t phase = 0;
     uint32_t armed = 0, armed_parity = 0;
-    bool ok = true;
+    bool ok = !Prob::no_loads(p);  // (timeout test: issue nothing)
     for (int j = 0; j < njobs && ok; ++j) {
       const TileJob tj = Prob::job(p, cluster, nclusters, j);
       const int m0 = tj.mb * P_TILE_M + static_cast<int>(rank) * 128;  // this CTA's A rows
@@ -226,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-    if (!ok || *abort) {
+    if ((!ok && !Prob::no_loads(p)) || *abort) {
       if (rank == 0)
         for (int s = 0; s < P_STAGES; ++s)
           if (armed & (1u << s)) mbar_wait_drain(&full[s], (armed_parity >> s) & 1u, 100000000ull);

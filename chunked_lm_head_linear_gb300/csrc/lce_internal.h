@@ -79,8 +79,10 @@ cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignor
 // Logits GEMM of a chunk: z [M, N] = A [M, K] B [N, K]^T with the FwdEpi
 // epilogue; a, b: K-major operand maps, c: the epilogue's store map (any valid
 // map if the mode stores nothing).
+// no_loads = 1 only for the timeout test (LCE_TEST_FORCE_TIMEOUT): no operand
+// loads are issued, so the MMA issuer's bounded wait runs out.
 cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, long long M, long long N,
-                          long long K, const FwdParams& ep, int num_sms, cudaStream_t s);
+                          long long K, const FwdParams& ep, int no_loads, int num_sms, cudaStream_t s);
 // Backward GEMMs of a chunk in one launch: dH_c = G W (ah: G K-major, bh: W
 // N-major, ch: dH store) and dW (+)= G^T B (aw: G M-major, bw: B N-major, cw:
 // dW store / reduce-add).

@@ -406,11 +406,13 @@ struct LogitsProb {
   struct Params {
     CUtensorMap a, b, c;
     int m_tiles, n_tiles, k_blocks;
+    int no_loads;   // timeout test only
     int* flags;
     FwdParams ep;
   };
   using State = FwdEpi::State;
   static __device__ __forceinline__ bool skip(const Params& p) { return FwdEpi::skip(p.ep); }
+  static __device__ __forceinline__ bool no_loads(const Params& p) { return p.no_loads != 0; }
   static __device__ __forceinline__ int* flags(const Params& p) { return p.flags; }
   static __device__ __forceinline__ int num_jobs(const Params& p, int c, int P) {
     const int tiles = p.m_tiles * p.n_tiles;
@@ -479,6 +481,7 @@ struct BwdProb {
     return s;
   }
   static __device__ __forceinline__ bool skip(const Params&) { return false; }
+  static __device__ __forceinline__ bool no_loads(const Params&) { return false; }
   static __device__ __forceinline__ int* flags(const Params& p) { return p.flags; }
   static __device__ __forceinline__ int num_jobs(const Params& p, int c, int P) {
     const Sched s = sched(p, c, P);
@@ -546,8 +549,9 @@ static cudaError_t launch_pair(const typename Prob::Params& p, int clusters, cud
 static int ceil_div_i(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
 
 cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, long long M, long long N,
-                          long long K, const FwdParams& ep, int num_sms, cudaStream_t s) {
+                          long long K, const FwdParams& ep, int no_loads, int num_sms, cudaStream_t s) {
   LogitsProb::Params p;
+  p.no_loads = no_loads;
   p.a = a;
   p.b = b;
   p.c = c;

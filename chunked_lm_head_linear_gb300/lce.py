@@ -31,11 +31,12 @@ LCE_ERR_TIMEOUT = 7
 LCE_MEAN, LCE_SUM = 0, 1
 LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD = 0, 1, 2
 LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
+LCE_TEST_FORCE_TIMEOUT = 0x7E57
 
 # Every symbol include/lce.h declares.
 EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
-            "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc")
+            "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk")
 LCE_KERNEL_KINDS = 10
 
 
@@ -94,6 +95,8 @@ def load(path: str | None = None):
         lib.lce_profile_begin.restype = I32
         lib.lce_profile_end.argtypes = [ctypes.POINTER(LceProfile)]
         lib.lce_profile_end.restype = I32
+        lib.lce_auto_chunk.argtypes = [I64, I64, I64, ctypes.c_size_t, OPT]
+        lib.lce_auto_chunk.restype = I64
         lib.lce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P]
         lib.lce_forward_noalloc.restype = I32
         lib.lce_kernel_name.argtypes = [I32]
@@ -106,8 +109,25 @@ def status_string(code: int) -> str:
     return load().lce_status_string(int(code)).decode()
 
 
+def auto_chunk(N: int, d: int, V: int, budget_bytes: int, opts: LceOpts | None = None) -> int:
+    """Largest chunk (multiple of 256 tokens, <= 4096) whose workspace fits the budget; 0 if none."""
+    return int(load().lce_auto_chunk(N, d, V, int(budget_bytes), ctypes.byref(opts) if opts is not None else None))
+
+
+def _resolve_chunk(chunk_tokens, N, d, V, device):
+    """chunk_tokens="auto": half of the device's free memory is the workspace budget."""
+    if chunk_tokens != "auto":
+        return chunk_tokens
+    import torch
+    free, _ = torch.cuda.mem_get_info(device)
+    c = auto_chunk(N, d, V, free // 2)
+    if c == 0:
+        raise LCEError(LCE_ERR_WORKSPACE, "auto_chunk: not even a 256-token chunk fits in half the free memory")
+    return c
+
+
 def make_opts(chunk_tokens=0, ignore_index=-100, reduction="mean", n_valid_override=-1,
-              accumulate_dW=False, sync_check=False) -> LceOpts:
+              accumulate_dW=False, sync_check=False, reserved=0) -> LceOpts:
     o = LceOpts()
     load().lce_opts_init(ctypes.byref(o))
     o.chunk_tokens = int(chunk_tokens)
@@ -116,6 +136,7 @@ def make_opts(chunk_tokens=0, ignore_index=-100, reduction="mean", n_valid_overr
     o.reduction = {"mean": LCE_MEAN, "sum": LCE_SUM}[reduction] if isinstance(reduction, str) else int(reduction)
     o.accumulate_dW = int(bool(accumulate_dW))
     o.sync_check = int(bool(sync_check))
+    o.reserved = int(reserved)
     return o
 
 
@@ -166,6 +187,8 @@ def lce_forward(H, W, y, *, workspace=None, stream=None, **opt_kw):
     """loss (fp32 [1]) and lse (fp32 [N]) of the token-level cross-entropy."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    if "chunk_tokens" in opt_kw:
+        opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
     ws = _workspace(LCE_OP_FORWARD, N, d, V, opts, H.device, workspace)
     loss = torch.empty(1, dtype=torch.float32, device=H.device)
@@ -181,6 +204,8 @@ def lce_backward(H, W, y, lse, grad_loss=None, *, dW=None, workspace=None, strea
     device fp32 scalar tensor or None (1.0)."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    if "chunk_tokens" in opt_kw:
+        opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
     ws = _workspace(LCE_OP_BACKWARD, N, d, V, opts, H.device, workspace)
     dH = torch.empty_like(H)
@@ -196,6 +221,8 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
     """loss, lse, dH, dW in one call."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    if "chunk_tokens" in opt_kw:
+        opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
     ws = _workspace(LCE_OP_FWD_BWD, N, d, V, opts, H.device, workspace)
     loss = torch.empty(1, dtype=torch.float32, device=H.device)

@@ -83,8 +83,16 @@ typedef struct lce_opts {
   int32_t accumulate_dW;    /* 0: dW = G^T H; 1: dW += G^T H (gradient accumulation) */
   int32_t sync_check;       /* 1: synchronise the stream at the end and turn device
                                status bits into the return code */
-  int32_t reserved;         /* must be 0 */
+  int32_t reserved;         /* 0, or LCE_TEST_FORCE_TIMEOUT (tests only, see below) */
 } lce_opts;
+
+/* Test value for lce_opts.reserved: lce_forward's logits kernel then loads
+ * no operands, so its bounded device waits run out (about 2 s); the kernel
+ * records LCE_DEVICE_TIMEOUT, releases its resources and returns, and the
+ * call reports LCE_ERR_TIMEOUT (with sync_check, or via
+ * lce_read_device_status). Outputs are meaningless. It exists to test the
+ * timeout path without faulting or hanging the GPU; other calls reject it. */
+#define LCE_TEST_FORCE_TIMEOUT 0x7E57
 
 /* Fill *opts with the defaults above. */
 void lce_opts_init(lce_opts* opts);
@@ -92,6 +100,15 @@ void lce_opts_init(lce_opts* opts);
 /* Bytes of device workspace one call of the given op needs (LCE_OP_*). opts
  * may be NULL (defaults). Returns 0 for invalid sizes. */
 size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opts* opts);
+
+/* Automatic chunk size ("XTuner V1 introduction", memory optimisation
+ * section: the loss graph is chunked automatically to bound its memory): the
+ * largest multiple of 256 tokens, at most 4096 and at most N rounded up to
+ * 256, whose LCE_OP_FWD_BWD workspace fits in budget_bytes (with opts'
+ * other fields). Larger chunks do not run faster on this GPU (W is read once
+ * per chunk either way), so 4096 is the cap. Returns 0 if not even 256
+ * tokens fit or the sizes are invalid. Host-only; touches no device. */
+int64_t lce_auto_chunk(int64_t N, int64_t d, int64_t V, size_t budget_bytes, const lce_opts* opts);
 
 /* Forward: loss [1] and lse [N] (fp32, device). lse of ignored rows is
  * computed too (the backward needs it for nothing, callers may use it).

@@ -134,3 +134,24 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load(str(tmp_path / "missing.so"))
         finally:
             mod._lib = saved
+
+
+def test_auto_chunk_policy(lib):
+    """The automatic chunk: largest multiple of 256 (<= 4096, <= N rounded up)
+    whose fused workspace fits the budget."""
+    V, d = 151936, 2048
+    big = 1 << 40
+    assert lce.auto_chunk(8192, d, V, big) == 4096
+    assert lce.auto_chunk(1000, d, V, big) == 1024
+    assert lce.auto_chunk(100, d, V, big) == 256
+    for budget_gb in (0.2, 0.5, 1.0, 2.0):
+        budget = int(budget_gb * 2**30)
+        C = lce.auto_chunk(65536, 4096, V, budget)
+        assert C % 256 == 0 and 0 < C <= 4096
+        ws = lce.workspace_size(lce.LCE_OP_FWD_BWD, 65536, 4096, V, lce.make_opts(chunk_tokens=C))
+        assert ws <= budget
+        if C < 4096:   # the next size up would not fit
+            assert lce.workspace_size(lce.LCE_OP_FWD_BWD, 65536, 4096, V,
+                                      lce.make_opts(chunk_tokens=C + 256)) > budget
+    assert lce.auto_chunk(65536, 4096, V, 1 << 20) == 0          # nothing fits in 1 MiB
+    assert lce.auto_chunk(8192, 7, V, big) == 0                  # invalid d

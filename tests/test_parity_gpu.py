@@ -163,6 +163,34 @@ def test_accumulate_dW(cuda_lib):
     assert rel_fro((dW - base).cpu().numpy(), ref["dW"]) <= TOL_GRAD
 
 
+def test_gradient_accumulation_over_micro_batches(cuda_lib):
+    """Micro-batches run one after the other with the denominator of the whole
+    batch and dW accumulated in place equal one call on the whole batch."""
+    torch = _torch()
+    inp = small_inputs(600, 128, 2000, seed=31)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    n = int((inp["y"] != oracle.IGNORE_INDEX).sum())
+    dW = torch.empty(2000, 128, dtype=torch.float32, device="cuda")
+    losses, dHs = [], []
+    for k, sl in enumerate((slice(0, 250), slice(250, 600))):
+        loss, _, dH, _ = cuda_lib.lce_fwd_bwd(H[sl], W, y[sl], dW=dW, n_valid_override=n, accumulate_dW=k > 0,
+                                              chunk_tokens=128, sync_check=True)
+        losses.append(loss.item())
+        dHs.append(dH)
+    assert abs(sum(losses) - ref["loss"]) <= TOL_LOSS * ref["loss"]
+    assert rel_fro(torch.cat(dHs).float().cpu().numpy(), ref["dH"]) <= TOL_GRAD
+    assert rel_fro(dW.cpu().numpy(), ref["dW"]) <= TOL_GRAD
+
+
+def test_auto_chunk(cuda_lib):
+    inp = small_inputs(700, 256, 4096, seed=33)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens="auto", sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
+
+
 def test_all_ignored_and_empty(cuda_lib):
     torch = _torch()
     inp = small_inputs(130, 64, 600, seed=3)
