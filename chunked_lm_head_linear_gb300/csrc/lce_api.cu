@@ -88,6 +88,11 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
     return at;
   };
   L.status = take(sizeof(DevStatus));
+  if (op == LCE_OP_VSHARD_COMBINE) {
+    L.loss_i = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+    L.total = off;
+    return L;
+  }
   const bool fwd = op == LCE_OP_FORWARD || op == LCE_OP_FWD_BWD;
   const bool bwd = op == LCE_OP_BACKWARD || op == LCE_OP_FWD_BWD;
   if (fwd) {
@@ -238,6 +243,8 @@ struct Call {
   const uint16_t* W;
   const int64_t* y;
   int64_t N, d, V;
+  int64_t V_total = 0;   // label range (V unless W is a vocabulary shard)
+  int64_t y_offset = 0;  // first vocabulary row of the shard
   lce_opts o;
   uint8_t* ws;
   Layout L;
@@ -270,6 +277,8 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   p.mode = a.mode;
   p.rows = static_cast<int>(rows);
   p.V = static_cast<int>(c.V);
+  p.V_total = static_cast<int>(c.V_total);
+  p.y_offset = c.y_offset;
   p.nparts = static_cast<int>(2 * c.L.T);
   p.ignore_index = c.o.ignore_index;
   p.y = c.y + c0;
@@ -307,20 +316,25 @@ int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* lo
 
 // dH_c = (g/n) [rowscale] (G W) and dW (+)= (g/n) G^T B, with G [rows, V] in
 // the chunk's tile buffer and B = H_c or Ht: one launch for both GEMMs.
-int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, uint16_t* dH, float* dW,
-          bool accumulate) {
+int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, void* dH, float* dW,
+          bool accumulate, bool dH_f32 = false) {
   const uint16_t* P = reinterpret_cast<const uint16_t*>(c.ws + c.L.P);
   CUtensorMap mG, mW, mdH, mGt, mB, mdW;
   LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kBoxRowsK));      // dH: A, K-major
   LCE_TRY(make_map(&mW, c.W, c.V, c.d, c.d, lce::kBoxRowsMN));        // dH: B, N-major
-  LCE_TRY(make_map(&mdH, dH + c0 * c.d, rows, c.d, c.d, kStoreRows));  // dH store
+  if (dH_f32)                                                           // dH store
+    LCE_TRY(make_map_t(&mdH, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<float*>(dH) + c0 * c.d, rows, c.d, c.d,
+                       32u, kStoreRows));
+  else
+    LCE_TRY(make_map(&mdH, static_cast<uint16_t*>(dH) + c0 * c.d, rows, c.d, c.d, kStoreRows));
   LCE_TRY(make_map(&mGt, P, rows, c.V, c.L.ldp, lce::kBoxRowsMN));    // dW: A, M-major
   LCE_TRY(make_map(&mB, B, rows, c.d, c.d, lce::kBoxRowsMN));          // dW: B, N-major
   LCE_TRY(make_map_t(&mdW, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, dW, c.V, c.d, c.d, 32u, kStoreRows));
   lce::DhParams dp;
   dp.rows = static_cast<int>(rows);
   dp.N = static_cast<int>(c.d);
-  dp.out = reinterpret_cast<__nv_bfloat16*>(dH + c0 * c.d);
+  dp.f32_out = dH_f32 ? 1 : 0;
+  dp.out = nullptr;  // written through the store map
   dp.ld = c.d;
   dp.rowscale = rowscale;
   dp.st = c.st;
@@ -340,14 +354,14 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
 
 // Backward of one chunk from a known lse: recompute the logits into the
 // exact gradient tile, then the two GEMMs.
-int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, uint16_t* dH, float* dW,
-                   bool accumulate) {
+int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, void* dH, float* dW, bool accumulate,
+                   bool dH_f32 = false) {
   LogitsArgs a;
   a.mode = lce::FWD_GRAD;
   a.lse_rows = lse + c0;
   a.P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
   LCE_TRY(logits_gemm(c, c0, rows, a));
-  return dh_dw(c, c0, rows, nullptr, c.H + c0 * c.d, dH, dW, accumulate);
+  return dh_dw(c, c0, rows, nullptr, c.H + c0 * c.d, dH, dW, accumulate, dH_f32);
 }
 
 // Forward and backward of one chunk without recomputing the logits: the
@@ -399,7 +413,7 @@ int prepare(const Call& c, const float* grad_loss) {
   int* guards = c.L.guard ? reinterpret_cast<int*>(c.ws + c.L.guard) : nullptr;
   const int nguards = c.L.guard ? static_cast<int>(c.L.chunks) : 0;
   return timed(c.s, K_PREPARE, 8.0 * static_cast<double>(c.N), [&] {
-    return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V), c.o.ignore_index, c.o.reduction,
+    return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V_total), c.o.ignore_index, c.o.reduction,
                                        c.o.n_valid_override, grad_loss, c.st, guards, nguards, c.s));
   });
 }
@@ -435,6 +449,8 @@ int begin(Call* c, int op, const void* H, const void* W, const int64_t* y, int64
   c->N = N;
   c->d = d;
   c->V = V;
+  c->V_total = V;
+  c->y_offset = 0;
   c->ws = static_cast<uint8_t*>(ws);
   c->st = reinterpret_cast<DevStatus*>(c->ws + c->L.status);
   c->s = static_cast<cudaStream_t>(stream);
@@ -458,7 +474,7 @@ size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opt
   lce_opts o;
   lce_opts_init(&o);
   if (opts) o = *opts;
-  if (op < LCE_OP_FORWARD || op > LCE_OP_FWD_BWD) return 0;
+  if (op < LCE_OP_FORWARD || op > LCE_OP_VSHARD_COMBINE) return 0;
   if (check_sizes(N, d, V, &o) != LCE_OK) return 0;
   return make_layout(op, N, d, V, &o).total;
 }
@@ -538,6 +554,101 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
                         c.o.accumulate_dW || c0 > 0));
   }
   LCE_TRY(finalize(c, loss_i, loss));
+  return finish(c);
+}
+
+static int shard_args(int64_t V_shard, int64_t vocab_offset, int64_t V_total) {
+  if (vocab_offset < 0 || V_shard <= 0 || V_total > (int64_t{1} << 31) - 1 || vocab_offset + V_shard > V_total)
+    return LCE_ERR_INVALID_ARG;
+  return LCE_OK;
+}
+
+int lce_vshard_forward_stats(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                             int64_t V_shard, int64_t vocab_offset, int64_t V_total, float* stats,
+                             const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  Call c;
+  LCE_TRY(begin(&c, LCE_OP_FORWARD, H, W_shard, y, N, d, V_shard, opts, ws, ws_bytes, stream));
+  LCE_TRY(shard_args(V_shard, vocab_offset, V_total));
+  if (c.o.reserved != 0 || (N > 0 && !stats)) return LCE_ERR_INVALID_ARG;
+  if (stats && !aligned(stats, 16)) return LCE_ERR_ALIGNMENT;
+  c.V_total = V_total;
+  c.y_offset = vocab_offset;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, nullptr));
+  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+    const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    LogitsArgs a;
+    a.mode = lce::FWD_STATS;
+    LCE_TRY(logits_gemm(c, c0, rows, a));
+    const double bytes = static_cast<double>(rows) * (16.0 * static_cast<double>(c.L.T) + 8 + 4 + 16);
+    LCE_TRY(timed(c.s, K_COMBINE, bytes, [&] {
+      return cuda_rc(lce::launch_shard_stats(reinterpret_cast<const float2*>(c.ws + c.L.partials),
+                                             static_cast<int>(2 * c.L.T), static_cast<int>(rows),
+                                             reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0,
+                                             vocab_offset, static_cast<int>(V_shard), static_cast<int>(V_total),
+                                             c.o.ignore_index, reinterpret_cast<float4*>(stats) + c0, c.s));
+    }));
+  }
+  return finish(c);
+}
+
+int lce_vshard_combine(const float* stats, int64_t R, const int64_t* y, int64_t N, int64_t V_total, float* lse,
+                       float* loss, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  Call c;
+  lce_opts_init(&c.o);
+  if (opts) c.o = *opts;
+  LCE_TRY(check_sizes(N, 8, V_total, &c.o));
+  if (R <= 0 || R > 4096 || !ws || !loss || (N > 0 && (!stats || !y || !lse)) || c.o.reserved != 0)
+    return LCE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || (stats && !aligned(stats, 16)) || (lse && !aligned(lse, 16)) || !aligned(loss, 4) ||
+      (y && !aligned(y, 16)))
+    return LCE_ERR_ALIGNMENT;
+  c.L = make_layout(LCE_OP_VSHARD_COMBINE, N, 8, V_total, &c.o);
+  if (ws_bytes < c.L.total) return LCE_ERR_WORKSPACE;
+  c.H = nullptr;
+  c.W = nullptr;
+  c.y = y;
+  c.N = N;
+  c.d = 8;
+  c.V = V_total;
+  c.V_total = V_total;
+  c.ws = static_cast<uint8_t*>(ws);
+  c.st = reinterpret_cast<DevStatus*>(c.ws + c.L.status);
+  c.s = static_cast<cudaStream_t>(stream);
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, nullptr));
+  float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
+  LCE_TRY(timed(c.s, K_COMBINE, static_cast<double>(N) * (16.0 * static_cast<double>(R) + 16), [&] {
+    return cuda_rc(lce::launch_shard_merge(reinterpret_cast<const float4*>(stats), static_cast<int>(R), N, y,
+                                           static_cast<int>(V_total), c.o.ignore_index, lse, loss_i, c.s));
+  }));
+  LCE_TRY(finalize(c, loss_i, loss));
+  return finish(c);
+}
+
+int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d, int64_t V_shard,
+                        int64_t vocab_offset, int64_t V_total, const float* lse, const float* grad_loss,
+                        float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
+                        void* stream) {
+  Call c;
+  LCE_TRY(begin(&c, LCE_OP_BACKWARD, H, W_shard, y, N, d, V_shard, opts, ws, ws_bytes, stream));
+  LCE_TRY(shard_args(V_shard, vocab_offset, V_total));
+  if (c.o.reserved != 0 || !dW_shard || (N > 0 && (!lse || !dH_partial))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(dW_shard, 16) || (dH_partial && !aligned(dH_partial, 16)) || (lse && !aligned(lse, 16)) ||
+      (grad_loss && !aligned(grad_loss, 4)))
+    return LCE_ERR_ALIGNMENT;
+  c.V_total = V_total;
+  c.y_offset = vocab_offset;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, grad_loss));
+  if (N == 0 && !c.o.accumulate_dW)
+    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V_shard * d), [&] {
+      return cuda_rc(cudaMemsetAsync(dW_shard, 0, sizeof(float) * static_cast<size_t>(V_shard * d), c.s));
+    }));
+  for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
+    const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    LCE_TRY(backward_chunk(c, c0, rows, lse, dH_partial, dW_shard, c.o.accumulate_dW || c0 > 0, true));
+  }
   return finish(c);
 }
 

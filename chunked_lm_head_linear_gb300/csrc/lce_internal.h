@@ -39,7 +39,9 @@ constexpr float kRefGuardNats = 60.f;
 struct FwdParams {
   int mode;
   int rows;              // rows of this chunk
-  int V;
+  int V;                 // vocabulary columns of this GEMM (a shard's size under vocabulary parallelism)
+  int V_total;           // label range: labels in [0, V_total) are valid
+  long long y_offset;    // label y sits in column y - y_offset (0 unless W is a vocabulary shard)
   int nparts;            // partials per row: two per 256-column vocabulary tile
   long long ignore_index;
   const int64_t* y;      // labels of this chunk
@@ -57,7 +59,8 @@ struct FwdParams {
 struct DhParams {
   int rows;              // rows of this chunk
   int N;                 // d
-  __nv_bfloat16* out;    // dH of this chunk, [rows, ld]
+  int f32_out;           // 1: fp32 output (a partial dH to be summed across vocabulary shards)
+  __nv_bfloat16* out;    // dH of this chunk, [rows, ld] (bf16, or fp32 when f32_out)
   long long ld;
   const float* rowscale; // optional per-row factor (nullptr: none)
   const DevStatus* st;   // gscale
@@ -96,6 +99,13 @@ cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, con
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s);
 cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, int d, __nv_bfloat16* Ht,
                           cudaStream_t s);
+// Vocabulary shards: per-row partial (max, sum-exp, target logit, has-target)
+// of this shard, and the fixed-order merge of R shards' partials.
+cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
+                               long long y_offset, int V_shard, int V_total, long long ignore_index, float4* stats,
+                               cudaStream_t s);
+cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const int64_t* y, int V_total,
+                               long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
 
 // GEMM tile geometry (must match the kernels): each CTA of a pair loads 128

@@ -48,8 +48,10 @@ struct FwdEpi {
     const int r = m0 + ctx.row0 + lane;
     const bool live = r < p.rows;
     const long long yr = live ? static_cast<long long>(p.y[r]) : p.ignore_index;
-    const bool valid = live && yr != p.ignore_index && yr >= 0 && yr < p.V;
-    const int ycol = valid ? static_cast<int>(yr - col0) : -1;
+    const bool valid = live && yr != p.ignore_index && yr >= 0 && yr < p.V_total;
+    // column of the label in this half tile (outside [0, 128) when the label is elsewhere)
+    const long long yc = valid ? yr - p.y_offset - col0 : -1;
+    const int ycol = (yc >= 0 && yc < EPI_COLS) ? static_cast<int>(yc) : -1;
     const int vlim = p.V - col0;  // columns >= vlim are past the vocabulary (warp-uniform)
     const int part = col0 / EPI_COLS;
 
@@ -142,7 +144,8 @@ struct FwdEpi {
   }
 };
 
-// dH tile: bf16(acc * g/n [* per-row factor]), stored by TMA into the chunk's dH rows.
+// dH tile: bf16(acc * g/n [* per-row factor]), stored by TMA into the chunk's dH
+// rows (fp32 instead when the result is a partial sum over vocabulary shards).
 struct DhEpi {
   using Params = DhParams;
   struct State {
@@ -157,6 +160,21 @@ struct DhEpi {
     if (m0 + ctx.row0 >= p.rows) return;  // all 32 rows of this warp are past the chunk
     float f = st.g;
     if (r < p.rows && p.rowscale != nullptr) f *= p.rowscale[r];
+    if (p.f32_out) {  // fp32 tiles of 32 columns, like the dW epilogue
+#pragma unroll 1
+      for (int u = 0; u < EPI_COLS / 32; ++u) {
+        if (col0 + u * 32 >= p.N) break;
+        stage_acquire(ctx);
+        float v[32];
+        tmem_ld_32x32b_x32(taddr + u * 32, v);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4*>(ctx.stage + stage_off(ctx.lane, q)) =
+              make_float4(v[4 * q] * f, v[4 * q + 1] * f, v[4 * q + 2] * f, v[4 * q + 3] * f);
+        stage_release(ctx, col0 + u * 32, m0 + ctx.row0, false);
+      }
+      return;
+    }
 #pragma unroll 1
     for (int u = 0; u < EPI_COLS / 64; ++u) {
       if (col0 + u * 64 >= p.N) break;
@@ -364,6 +382,59 @@ __global__ void __launch_bounds__(256) k_hscale(const uint4* __restrict__ H, con
     }
     Ht[i] = make_uint4(o[0], o[1], o[2], o[3]);
   }
+}
+
+// One warp per row: this vocabulary shard's (max, sum-exp) over its columns,
+// its logit of the label if the label lies in the shard, and whether it does.
+__global__ void __launch_bounds__(256) k_shard_stats(const float2* __restrict__ partials, int T, int rows,
+                                                     const float* __restrict__ ztgt, const int64_t* __restrict__ y,
+                                                     long long y_offset, int V_shard, int V_total,
+                                                     long long ignore_index, float4* __restrict__ stats) {
+  const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float m = -INFINITY, s = 0.f;
+  const float2* pr = partials + static_cast<long long>(r) * T;
+  for (int t = lane; t < T; t += 32) {
+    const float2 q = pr[t];
+    merge_ms(m, s, q.x, q.y);
+  }
+  for (int off = 16; off > 0; off >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
+    merge_ms(m, s, m2, s2);
+  }
+  if (lane == 0) {
+    const long long yr = y[r];
+    const bool valid = yr != ignore_index && yr >= 0 && yr < V_total;
+    const long long col = yr - y_offset;
+    const bool here = valid && col >= 0 && col < V_shard;
+    stats[r] = make_float4(m, s, here ? ztgt[r] : 0.f, here ? 1.f : 0.f);
+  }
+}
+
+// Merge R shards' row statistics in shard order: M = max_r m_r,
+// S = sum_r s_r e^{m_r - M}, lse = M + log S, z_y from the shard that holds
+// the label; loss_i = lse - z_y for valid rows. One thread per row.
+__global__ void __launch_bounds__(256) k_shard_merge(const float4* __restrict__ stats, int R, long long N,
+                                                     const int64_t* __restrict__ y, int V_total,
+                                                     long long ignore_index, float* __restrict__ lse,
+                                                     float* __restrict__ loss_i) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= N) return;
+  float M = -INFINITY;
+  for (int r = 0; r < R; ++r) M = fmaxf(M, stats[r * N + i].x);
+  float S = 0.f, zt = 0.f;
+  for (int r = 0; r < R; ++r) {
+    const float4 q = stats[r * N + i];
+    if (q.y > 0.f) S += q.y * exp2f((q.x - M) * kLog2e);
+    zt += q.w > 0.f ? q.z : 0.f;
+  }
+  const float l = M + logf(S);
+  lse[i] = l;
+  const long long yr = y[i];
+  const bool valid = yr != ignore_index && yr >= 0 && yr < V_total;
+  loss_i[i] = valid ? l - zt : 0.f;
 }
 
 // loss = (sum_i loss_i) * lscale, fp64 accumulation in a fixed order.
@@ -632,6 +703,24 @@ cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, 
   if (blocks > 152 * 8) blocks = 152 * 8;
   k_hscale<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(H), alpha, groups, d / 8,
                                                     reinterpret_cast<uint4*>(Ht));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
+                               long long y_offset, int V_shard, int V_total, long long ignore_index, float4* stats,
+                               cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int grid = (rows + 7) / 8;
+  k_shard_stats<<<grid, 256, 0, s>>>(partials, nparts, rows, ztgt, y, y_offset, V_shard, V_total, ignore_index,
+                                     stats);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const int64_t* y, int V_total,
+                               long long ignore_index, float* lse, float* loss_i, cudaStream_t s) {
+  if (N <= 0) return cudaSuccess;
+  const long long grid = (N + 255) / 256;
+  k_shard_merge<<<static_cast<unsigned>(grid), 256, 0, s>>>(stats, R, N, y, V_total, ignore_index, lse, loss_i);
   return cudaGetLastError();
 }
 

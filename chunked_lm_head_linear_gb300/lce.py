@@ -29,14 +29,15 @@ LCE_ERR_LABEL_RANGE = 6
 LCE_ERR_TIMEOUT = 7
 
 LCE_MEAN, LCE_SUM = 0, 1
-LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD = 0, 1, 2
+LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD, LCE_OP_VSHARD_COMBINE = 0, 1, 2, 3
 LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
 LCE_TEST_FORCE_TIMEOUT = 0x7E57
 
 # Every symbol include/lce.h declares.
 EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
-            "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk")
+            "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk",
+            "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward")
 LCE_KERNEL_KINDS = 10
 
 
@@ -95,6 +96,12 @@ def load(path: str | None = None):
         lib.lce_profile_begin.restype = I32
         lib.lce_profile_end.argtypes = [ctypes.POINTER(LceProfile)]
         lib.lce_profile_end.restype = I32
+        lib.lce_vshard_forward_stats.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_vshard_forward_stats.restype = I32
+        lib.lce_vshard_combine.argtypes = [P, I64, P, I64, I64, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_vshard_combine.restype = I32
+        lib.lce_vshard_backward.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_vshard_backward.restype = I32
         lib.lce_auto_chunk.argtypes = [I64, I64, I64, ctypes.c_size_t, OPT]
         lib.lce_auto_chunk.restype = I64
         lib.lce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P]
@@ -259,3 +266,55 @@ def profile_end() -> dict:
         name = load().lce_kernel_name(k).decode()
         out[name] = {"launches": p.launches[k], "ms": p.ms[k], "work": p.work[k]}
     return out
+
+
+# ---------------------------------------------------------------------------
+# Vocabulary-parallel pieces (W split by rows; see include/lce.h)
+# ---------------------------------------------------------------------------
+def lce_vshard_forward_stats(H, W_shard, y, vocab_offset: int, V_total: int, *, workspace=None, stream=None,
+                             **opt_kw):
+    """Per-row (max, sum-exp, label logit, has-label) of this vocabulary shard: fp32 [N, 4]."""
+    import torch
+    N, d, Vs = _check_inputs(H, W_shard, y)
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_FORWARD, N, d, Vs, opts, H.device, workspace)
+    stats = torch.empty((max(N, 1), 4), dtype=torch.float32, device=H.device)[:N]
+    rc = load().lce_vshard_forward_stats(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
+                                         _ptr(stats), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_vshard_forward_stats")
+    return stats
+
+
+def lce_vshard_combine(stats_all, y, V_total: int, *, workspace=None, stream=None, **opt_kw):
+    """Merge the shards' statistics [R, N, 4] (rank order) into lse [N] and the loss [1]."""
+    import torch
+    R, N = int(stats_all.shape[0]), int(stats_all.shape[1])
+    if not (stats_all.is_cuda and stats_all.dtype == torch.float32 and stats_all.is_contiguous()):
+        raise ValueError("stats_all must be a contiguous fp32 CUDA tensor [R, N, 4]")
+    opts = make_opts(**opt_kw)
+    need = workspace_size(LCE_OP_VSHARD_COMBINE, N, 8, V_total, opts)
+    ws = workspace if workspace is not None and workspace.numel() >= need else \
+        torch.empty(need, dtype=torch.uint8, device=stats_all.device)
+    lse = torch.empty(max(N, 1), dtype=torch.float32, device=stats_all.device)[:N]
+    loss = torch.empty(1, dtype=torch.float32, device=stats_all.device)
+    rc = load().lce_vshard_combine(_ptr(stats_all), R, _ptr(y), N, int(V_total), _ptr(lse), _ptr(loss),
+                                   ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_vshard_combine")
+    return loss, lse
+
+
+def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, grad_loss=None, *, dW=None,
+                        workspace=None, stream=None, **opt_kw):
+    """This shard's dW [V_shard, d] and its fp32 partial dH [N, d] (sum over shards = dH)."""
+    import torch
+    N, d, Vs = _check_inputs(H, W_shard, y)
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_BACKWARD, N, d, Vs, opts, H.device, workspace)
+    dH = torch.empty((N, d), dtype=torch.float32, device=H.device)
+    if dW is None:
+        dW = torch.empty((Vs, d), dtype=torch.float32, device=H.device)
+    rc = load().lce_vshard_backward(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
+                                    _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW), ctypes.byref(opts), _ptr(ws),
+                                    ws.numel(), _stream(stream))
+    _raise(rc, "lce_vshard_backward")
+    return dH, dW

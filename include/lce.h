@@ -69,6 +69,7 @@ extern "C" {
 #define LCE_OP_FORWARD 0
 #define LCE_OP_BACKWARD 1
 #define LCE_OP_FWD_BWD 2
+#define LCE_OP_VSHARD_COMBINE 3
 
 /* device status bits returned by lce_read_device_status */
 #define LCE_DEVICE_LABEL_RANGE 1
@@ -148,6 +149,38 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
  * overwrites what it reads, and lce_read_device_status() does not apply. */
 int lce_forward_noalloc(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
                         float* loss, float* lse, const lce_opts* opts, void* stream);
+
+/*
+ * Vocabulary-parallel use (W split by rows over R ranks; each rank holds
+ * W_shard = W[vocab_offset : vocab_offset + V_shard], all of H and the global
+ * labels). The token-level cross-entropy needs, per token, the log-sum-exp
+ * over the whole vocabulary; it is assembled from per-shard statistics with
+ * the streaming max / sum-exp rule ("MindSpeed fusion optimisation: principles
+ * and practice", section 3.2, applied across vocabulary shards):
+ *   1. lce_vshard_forward_stats on each rank -> stats [N, 4] fp32 (device):
+ *      (max over the shard, sum of exp(z - max) over the shard, the label's
+ *      logit if the label lies in the shard else 0, 1 if it does else 0);
+ *   2. the caller gathers the R stats arrays into one [R, N, 4] array in rank
+ *      order (an all-gather), and every rank calls lce_vshard_combine ->
+ *      lse [N] and loss [1] (merged in rank order: identical on all ranks);
+ *   3. lce_vshard_backward on each rank with that lse -> dW_shard
+ *      [V_shard, d] (complete for the shard) and dH_partial [N, d] fp32, whose
+ *      sum over ranks (an all-reduce) is dH.
+ * Labels are global ids in [0, V_total) or ignore_index; the denominator n is
+ * the count of valid labels (all ranks see all labels) unless overridden.
+ * Workspaces: lce_workspace_size(LCE_OP_FORWARD / LCE_OP_BACKWARD, N, d,
+ * V_shard, opts) and (LCE_OP_VSHARD_COMBINE, N, d, V_total, opts).
+ * Requirements: 0 <= vocab_offset, vocab_offset + V_shard <= V_total.
+ */
+int lce_vshard_forward_stats(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                             int64_t V_shard, int64_t vocab_offset, int64_t V_total, float* stats,
+                             const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
+int lce_vshard_combine(const float* stats, int64_t R, const int64_t* y, int64_t N, int64_t V_total, float* lse,
+                       float* loss, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
+int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d, int64_t V_shard,
+                        int64_t vocab_offset, int64_t V_total, const float* lse, const float* grad_loss,
+                        float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /* Synchronise the stream and copy the workspace's device status bits
  * (LCE_DEVICE_*) of the last call that used ws into *flags. */

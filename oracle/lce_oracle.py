@@ -248,3 +248,57 @@ def dW_rows_f64(H, W, y, lse, vrows, scale, *, ignore_index=IGNORE_INDEX):
         p[valid & (y == v), j] -= 1.0
     G = p * (valid * scale)[:, None]
     return G.T @ H64
+
+
+# ---------------------------------------------------------------------------
+# Vocabulary shards: the per-shard statistics and their merge, written from
+# the streaming max / sum-exp rule ("MindSpeed fusion optimisation: principles
+# and practice", section 3.2), with the shards playing the role of blocks.
+# ---------------------------------------------------------------------------
+
+def vshard_stats_f64(H, W_shard, y, vocab_offset, V_total, *, ignore_index=IGNORE_INDEX):
+    """Per row of this shard: m = max_v z, s = sum_v exp(z - m), the label's logit
+    if the label lies in the shard, and 1/0 for whether it does. [N, 4] fp64."""
+    H = np.asarray(H, dtype=np.float64)
+    Ws = np.asarray(W_shard, dtype=np.float64)
+    y = np.asarray(y, dtype=np.int64)
+    z = H @ Ws.T
+    m = z.max(axis=1)
+    s = np.exp(z - m[:, None]).sum(axis=1)
+    valid = (y != ignore_index) & (y >= 0) & (y < V_total)
+    col = y - vocab_offset
+    here = valid & (col >= 0) & (col < Ws.shape[0])
+    zt = np.where(here, z[np.arange(len(y)), np.where(here, col, 0)], 0.0)
+    return np.stack([m, s, zt, here.astype(np.float64)], axis=1)
+
+
+def vshard_merge_f64(stats_all, y, *, ignore_index=IGNORE_INDEX, V_total=None, n_valid_override=-1):
+    """Merge [R, N, 4] shard statistics: M = max_r m_r, S = sum_r s_r exp(m_r - M),
+    lse = M + log S, z_y from the shard that has the label. Returns (loss, lse)."""
+    st = np.asarray(stats_all, dtype=np.float64)
+    y = np.asarray(y, dtype=np.int64)
+    M = st[:, :, 0].max(axis=0)
+    S = (st[:, :, 1] * np.exp(st[:, :, 0] - M[None, :])).sum(axis=0)
+    lse = M + np.log(S)
+    zt = (st[:, :, 2] * st[:, :, 3]).sum(axis=0)
+    valid = y != ignore_index
+    if V_total is not None:
+        valid &= (y >= 0) & (y < V_total)
+    n = int(valid.sum()) if n_valid_override < 0 else int(n_valid_override)
+    loss_i = np.where(valid, lse - zt, 0.0)
+    return (math.fsum(loss_i.tolist()) / n if n else 0.0), lse
+
+
+def vshard_backward_f64(H, W_shard, y, vocab_offset, lse, scale, *, ignore_index=IGNORE_INDEX):
+    """This shard's dW rows and its part of dH, from the full-vocabulary lse."""
+    H = np.asarray(H, dtype=np.float64)
+    Ws = np.asarray(W_shard, dtype=np.float64)
+    y = np.asarray(y, dtype=np.int64)
+    z = H @ Ws.T
+    p = np.exp(z - np.asarray(lse)[:, None])
+    valid = y != ignore_index
+    col = y - vocab_offset
+    here = valid & (col >= 0) & (col < Ws.shape[0])
+    p[np.nonzero(here)[0], col[here]] -= 1.0
+    G = p * (valid * scale)[:, None]
+    return G @ Ws, G.T @ H

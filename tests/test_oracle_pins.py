@@ -365,3 +365,21 @@ def test_sampled_helpers_match_full_oracle():
     assert _rel(oracle.dH_rows_f64(H, W, y, rows, scale), full["dH"][rows]) < 1e-13
     vrows = np.array([0, 1, 350, 699])
     assert _rel(oracle.dW_rows_f64(H, W, y, full["lse"], vrows, scale), full["dW"][vrows]) < 1e-13
+
+
+@pytest.mark.parametrize("cuts", [(0, 13, 40), (0, 1, 2, 40), (0, 20, 33, 39, 40)])
+def test_vocab_shards_merge_to_the_whole(cuts):
+    """Per-shard (max, sum-exp, label logit) merged with the streaming rule, and
+    per-shard backward pieces summed, equal the unsharded definition -- also for
+    shards that hold no label at all."""
+    rng = np.random.default_rng(sum(cuts))
+    H, W, y = _rand(rng, 37, 9, 40, sw=1.5)
+    whole = oracle.lce_f64(H, W, y)
+    stats = np.stack([oracle.vshard_stats_f64(H, W[a:b], y, a, 40) for a, b in zip(cuts[:-1], cuts[1:])])
+    loss, lse = oracle.vshard_merge_f64(stats, y, V_total=40)
+    assert loss == pytest.approx(whole["loss"], rel=1e-13)
+    np.testing.assert_allclose(lse, whole["lse"], rtol=1e-14)
+    scale, _ = oracle.grad_scale(y)
+    parts = [oracle.vshard_backward_f64(H, W[a:b], y, a, lse, scale) for a, b in zip(cuts[:-1], cuts[1:])]
+    assert _rel(sum(p[0] for p in parts), whole["dH"]) < 1e-13
+    assert _rel(np.vstack([p[1] for p in parts]), whole["dW"]) < 1e-13

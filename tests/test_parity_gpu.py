@@ -191,6 +191,33 @@ def test_auto_chunk(cuda_lib):
     check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
 
 
+@pytest.mark.parametrize("cuts,chunk", [((0, 1000, 2600, 4099), 0), ((0, 257, 4099), 200), ((0, 4000, 4099), 512)])
+def test_vocab_shards_on_one_gpu(cuda_lib, cuts, chunk):
+    """Vocabulary-parallel pieces run shard after shard on one GPU: merged
+    statistics give the full lse and loss, partial dH sum to dH, and the
+    shards' dW rows stack to dW (shards of ragged sizes, one with few labels)."""
+    torch = _torch()
+    inp = small_inputs(700, 264, 4099, seed=37, sigma_w=0.05)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    shards = list(zip(cuts[:-1], cuts[1:]))
+    stats = [cuda_lib.lce_vshard_forward_stats(H, W[a:b], y, a, 4099, chunk_tokens=chunk, sync_check=True)
+             for a, b in shards]
+    loss, lse = cuda_lib.lce_vshard_combine(torch.stack(stats).contiguous(), y, 4099, sync_check=True)
+    dH = torch.zeros(700, 264, dtype=torch.float32, device="cuda")
+    dWs = []
+    for a, b in shards:
+        dHp, dWp = cuda_lib.lce_vshard_backward(H, W[a:b].contiguous(), y, a, 4099, lse, chunk_tokens=chunk,
+                                                sync_check=True)
+        dH += dHp
+        dWs.append(dWp)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), dH.cpu().numpy().astype(np.float64),
+                         torch.cat(dWs).cpu().numpy())
+    # the fused single-device call and the sharded route agree on lse
+    _, lse_full, _, _ = cuda_lib.lce_fwd_bwd(H, W, y, sync_check=True)
+    assert ((lse - lse_full).abs() / lse_full.abs()).max().item() <= TOL_LSE
+
+
 def test_all_ignored_and_empty(cuda_lib):
     torch = _torch()
     inp = small_inputs(130, 64, 600, seed=3)
