@@ -21,7 +21,7 @@ LIB = os.path.join(BUILD, "liblce.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
           "-I" + os.path.join(ROOT, "include")]
-SOURCES = ["lce_kernels.cu", "lce_api.cu", "lce_noalloc.cu"]
+SOURCES = ["lce_kernels.cu", "lce_api.cu", "lce_noalloc.cu", "lce_rmsnorm.cu"]
 
 
 def nvcc() -> str:

@@ -113,6 +113,33 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
   return L;
 }
 
+// lce_norm_fwd_bwd: the fused linear-CE workspace, then H, rstd, dH and the
+// RMSNorm backward's partial rows.
+struct NormLayout {
+  Layout lce;
+  size_t H = 0, rstd = 0, dH = 0, part = 0, total = 0;
+};
+
+NormLayout norm_layout(int64_t N, int64_t d, int64_t V, const lce_opts* o) {
+  NormLayout L;
+  L.lce = make_layout(LCE_OP_FWD_BWD, N, d, V, o);
+  size_t off = L.lce.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  const size_t nd = static_cast<size_t>(N > 0 ? N : 1) * static_cast<size_t>(d);
+  L.H = take(2 * nd);
+  L.rstd = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
+  L.dH = take(2 * nd);
+  L.part = take(sizeof(float) * static_cast<size_t>(lce::rmsnorm_bwd_blocks(N > 0 ? N : 1)) * static_cast<size_t>(d));
+  L.total = off;
+  return L;
+}
+
+constexpr int64_t kNormMaxD = 32768;  // the norm backward keeps a row of dw partials in shared memory
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int check_sizes(int64_t N, int64_t d, int64_t V, const lce_opts* o) {
@@ -189,7 +216,7 @@ enum Kind : int {
   K_GEMM_BWD = 4,       // dH and dW GEMMs of a chunk (one launch)
   K_RESERVED = 5,
   K_FINALIZE = 6,
-  K_OTHER = 7,          // memsets and the guard-conditional FWD_GRAD (work counted as 0)
+  K_OTHER = 7,          // memsets, the guard-conditional FWD_GRAD (work counted as 0), RMSNorm kernels
   K_LOGITS_REF = 8,
   K_HSCALE = 9,
 };
@@ -474,8 +501,9 @@ size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opt
   lce_opts o;
   lce_opts_init(&o);
   if (opts) o = *opts;
-  if (op < LCE_OP_FORWARD || op > LCE_OP_VSHARD_COMBINE) return 0;
+  if (op < LCE_OP_FORWARD || op > LCE_OP_NORM_FWD_BWD) return 0;
   if (check_sizes(N, d, V, &o) != LCE_OK) return 0;
+  if (op == LCE_OP_NORM_FWD_BWD) return norm_layout(N, d, V, &o).total;
   return make_layout(op, N, d, V, &o).total;
 }
 
@@ -650,6 +678,75 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
     LCE_TRY(backward_chunk(c, c0, rows, lse, dH_partial, dW_shard, c.o.accumulate_dW || c0 > 0, true));
   }
   return finish(c);
+}
+
+size_t lce_rmsnorm_workspace_size(int64_t N, int64_t d) {
+  if (N < 0 || d <= 0 || d % 8 != 0 || d > kNormMaxD) return 0;
+  return align256(sizeof(float) * static_cast<size_t>(lce::rmsnorm_bwd_blocks(N > 0 ? N : 1)) *
+                  static_cast<size_t>(d));
+}
+
+int lce_rmsnorm_forward(const void* x, const float* w, int64_t N, int64_t d, float eps, void* H, float* rstd,
+                        void* stream) {
+  if (N < 0 || d <= 0 || d % 8 != 0 || d > kNormMaxD || !(eps >= 0.f)) return LCE_ERR_INVALID_ARG;
+  if (!w || (N > 0 && (!x || !H || !rstd))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || (x && !aligned(x, 16)) || (H && !aligned(H, 16)) || (rstd && !aligned(rstd, 4)))
+    return LCE_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  LCE_TRY(device_check(&dev));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return timed(s, K_OTHER, 4.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N), [&] {
+    return cuda_rc(lce::launch_rmsnorm_fwd(x, w, N, static_cast<int>(d), eps, H, rstd, s));
+  });
+}
+
+int lce_rmsnorm_backward(const void* x, const float* w, const float* rstd, const void* dH, int64_t N, int64_t d,
+                         void* dx, float* dw, void* ws, size_t ws_bytes, void* stream) {
+  if (N < 0 || d <= 0 || d % 8 != 0 || d > kNormMaxD) return LCE_ERR_INVALID_ARG;
+  if (!w || !dw || !ws || (N > 0 && (!x || !rstd || !dH || !dx))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(ws, 256) || (x && !aligned(x, 16)) || (dH && !aligned(dH, 16)) ||
+      (dx && !aligned(dx, 16)) || (rstd && !aligned(rstd, 4)) || !aligned(dw, 4))
+    return LCE_ERR_ALIGNMENT;
+  if (ws_bytes < lce_rmsnorm_workspace_size(N, d)) return LCE_ERR_WORKSPACE;
+  DeviceInfo dev;
+  LCE_TRY(device_check(&dev));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return timed(s, K_OTHER, 6.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N + d), [&] {
+    return cuda_rc(lce::launch_rmsnorm_bwd(x, w, rstd, dH, N, static_cast<int>(d), dx, dw, static_cast<float*>(ws),
+                                           s));
+  });
+}
+
+int lce_norm_fwd_bwd(const void* x, const float* w_norm, float eps, const void* W, const int64_t* y, int64_t N,
+                     int64_t d, int64_t V, const float* grad_loss, float* loss, float* lse, void* dx, float* dw_norm,
+                     float* dW, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  lce_opts o;
+  lce_opts_init(&o);
+  if (opts) o = *opts;
+  LCE_TRY(check_sizes(N, d, V, &o));
+  if (d > kNormMaxD || !(eps >= 0.f) || o.reserved != 0) return LCE_ERR_INVALID_ARG;
+  if (!w_norm || !dw_norm || !ws || (N > 0 && (!x || !dx))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(ws, 256) || !aligned(w_norm, 16) || !aligned(dw_norm, 4) || (x && !aligned(x, 16)) ||
+      (dx && !aligned(dx, 16)))
+    return LCE_ERR_ALIGNMENT;
+  const NormLayout L = norm_layout(N, d, V, &o);
+  if (ws_bytes < L.total) return LCE_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  void* H = base + L.H;
+  float* rstd = reinterpret_cast<float*>(base + L.rstd);
+  void* dH = base + L.dH;
+  LCE_TRY(lce_rmsnorm_forward(x, w_norm, N, d, eps, H, rstd, stream));
+  lce_opts inner = o;
+  inner.sync_check = 0;
+  LCE_TRY(lce_fwd_bwd(H, W, y, N, d, V, grad_loss, loss, lse, dH, dW, &inner, ws, L.lce.total, stream));
+  LCE_TRY(lce_rmsnorm_backward(x, w_norm, rstd, dH, N, d, dx, dw_norm, base + L.part, L.total - L.part, stream));
+  if (!o.sync_check) return LCE_OK;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LCE_ERR_CUDA;
+  int flags = 0;
+  if (cudaMemcpy(&flags, base, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
+  if (flags & lce::kFlagTimeout) return LCE_ERR_TIMEOUT;
+  if (flags & lce::kFlagLabelRange) return LCE_ERR_LABEL_RANGE;
+  return LCE_OK;
 }
 
 int lce_read_device_status(const void* ws, void* stream, int* flags) {

@@ -106,6 +106,13 @@ cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, con
                                cudaStream_t s);
 cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const int64_t* y, int V_total,
                                long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
+// Final zero-centred RMSNorm (lce_rmsnorm.cu). rmsnorm_bwd_blocks(N) partial
+// rows of d floats are the backward's scratch.
+int rmsnorm_bwd_blocks(long long N);
+cudaError_t launch_rmsnorm_fwd(const void* x, const float* w, long long N, int d, float eps, void* H, float* rstd,
+                               cudaStream_t s);
+cudaError_t launch_rmsnorm_bwd(const void* x, const float* w, const float* rstd, const void* dH, long long N, int d,
+                               void* dx, float* dw, float* part, cudaStream_t s);
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
 
 // GEMM tile geometry (must match the kernels): each CTA of a pair loads 128

@@ -29,7 +29,7 @@ LCE_ERR_LABEL_RANGE = 6
 LCE_ERR_TIMEOUT = 7
 
 LCE_MEAN, LCE_SUM = 0, 1
-LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD, LCE_OP_VSHARD_COMBINE = 0, 1, 2, 3
+LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD, LCE_OP_VSHARD_COMBINE, LCE_OP_NORM_FWD_BWD = 0, 1, 2, 3, 4
 LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
 LCE_TEST_FORCE_TIMEOUT = 0x7E57
 
@@ -37,7 +37,8 @@ LCE_TEST_FORCE_TIMEOUT = 0x7E57
 EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward", "lce_fwd_bwd",
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
             "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk",
-            "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward")
+            "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward",
+            "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd")
 LCE_KERNEL_KINDS = 10
 
 
@@ -102,6 +103,15 @@ def load(path: str | None = None):
         lib.lce_vshard_combine.restype = I32
         lib.lce_vshard_backward.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, OPT, P, ctypes.c_size_t, P]
         lib.lce_vshard_backward.restype = I32
+        F32 = ctypes.c_float
+        lib.lce_rmsnorm_workspace_size.argtypes = [I64, I64]
+        lib.lce_rmsnorm_workspace_size.restype = ctypes.c_size_t
+        lib.lce_rmsnorm_forward.argtypes = [P, P, I64, I64, F32, P, P, P]
+        lib.lce_rmsnorm_forward.restype = I32
+        lib.lce_rmsnorm_backward.argtypes = [P, P, P, P, I64, I64, P, P, P, ctypes.c_size_t, P]
+        lib.lce_rmsnorm_backward.restype = I32
+        lib.lce_norm_fwd_bwd.argtypes = [P, P, F32, P, P, I64, I64, I64, P, P, P, P, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_norm_fwd_bwd.restype = I32
         lib.lce_auto_chunk.argtypes = [I64, I64, I64, ctypes.c_size_t, OPT]
         lib.lce_auto_chunk.restype = I64
         lib.lce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P]
@@ -318,3 +328,64 @@ def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, gra
                                     ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_backward")
     return dH, dW
+
+
+# ---------------------------------------------------------------------------
+# Final zero-centred RMSNorm (see include/lce.h)
+# ---------------------------------------------------------------------------
+def _check_norm(x, w):
+    import torch
+    if not (x.is_cuda and w.is_cuda) or x.dtype != torch.bfloat16 or w.dtype != torch.float32:
+        raise ValueError("x must be a bf16 CUDA tensor [N, d], w an fp32 CUDA tensor [d]")
+    if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1] or not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("shapes must be x [N, d], w [d], contiguous")
+    return x.shape[0], x.shape[1]
+
+
+def lce_rmsnorm_forward(x, w, eps=1e-6, *, stream=None):
+    """H = bf16(x / rms(x) * (1 + w)) and the per-row 1/rms (fp32)."""
+    import torch
+    N, d = _check_norm(x, w)
+    H = torch.empty_like(x)
+    rstd = torch.empty(max(N, 1), dtype=torch.float32, device=x.device)[:N]
+    _raise(load().lce_rmsnorm_forward(_ptr(x), _ptr(w), N, d, float(eps), _ptr(H), _ptr(rstd), _stream(stream)),
+           "lce_rmsnorm_forward")
+    return H, rstd
+
+
+def lce_rmsnorm_backward(x, w, rstd, dH, *, stream=None):
+    """dx (bf16 [N, d]) and dw (fp32 [d]) of the zero-centred RMSNorm."""
+    import torch
+    N, d = _check_norm(x, w)
+    dx = torch.empty_like(x)
+    dw = torch.empty(d, dtype=torch.float32, device=x.device)
+    need = int(load().lce_rmsnorm_workspace_size(N, d))
+    if need == 0:
+        raise LCEError(LCE_ERR_INVALID_ARG, "lce_rmsnorm_workspace_size")
+    ws = torch.empty(need, dtype=torch.uint8, device=x.device)
+    _raise(load().lce_rmsnorm_backward(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dH), N, d, _ptr(dx), _ptr(dw), _ptr(ws),
+                                       ws.numel(), _stream(stream)), "lce_rmsnorm_backward")
+    return dx, dw
+
+
+def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, workspace=None, stream=None, **opt_kw):
+    """Final norm + LM head + cross-entropy, forward and backward:
+    returns loss, lse, dx, dw_norm, dW."""
+    import torch
+    N, d = _check_norm(x, w_norm)
+    if W.dim() != 2 or W.shape[1] != d or W.dtype != torch.bfloat16 or not W.is_contiguous():
+        raise ValueError("W must be a contiguous bf16 [V, d] tensor")
+    V = W.shape[0]
+    opts = make_opts(**opt_kw)
+    ws = _workspace(LCE_OP_NORM_FWD_BWD, N, d, V, opts, x.device, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    lse = torch.empty(max(N, 1), dtype=torch.float32, device=x.device)[:N]
+    dx = torch.empty_like(x)
+    dw_norm = torch.empty(d, dtype=torch.float32, device=x.device)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=x.device)
+    rc = load().lce_norm_fwd_bwd(_ptr(x), _ptr(w_norm), float(eps), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss),
+                                 _ptr(loss), _ptr(lse), _ptr(dx), _ptr(dw_norm), _ptr(dW), ctypes.byref(opts),
+                                 _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_norm_fwd_bwd")
+    return loss, lse, dx, dw_norm, dW

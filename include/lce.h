@@ -70,6 +70,7 @@ extern "C" {
 #define LCE_OP_BACKWARD 1
 #define LCE_OP_FWD_BWD 2
 #define LCE_OP_VSHARD_COMBINE 3
+#define LCE_OP_NORM_FWD_BWD 4
 
 /* device status bits returned by lce_read_device_status */
 #define LCE_DEVICE_LABEL_RANGE 1
@@ -181,6 +182,30 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
                         int64_t vocab_offset, int64_t V_total, const float* lse, const float* grad_loss,
                         float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
                         void* stream);
+
+/*
+ * The final zero-centred RMSNorm that produces H ("XTuner on Ascend 910C:
+ * Qwen3.5-2B training optimisation", section 3.1.1: one pass over the bf16
+ * input with the (1 + w) scale folded into an fp32 gamma and one bf16
+ * rounding of the output):
+ *   r_i = 1 / sqrt(mean_k x_ik^2 + eps),  H_ik = bf16(x_ik r_i (1 + w_k)).
+ * x, H, dH, dx: [N, d] bf16 row-major; w (the zero-centred weight), dw: [d]
+ * fp32; rstd: [N] fp32 (r_i, saved by the forward for the backward).
+ * d % 8 == 0 and d <= 32768; x, H, dH, dx, w 16-byte aligned.
+ * lce_rmsnorm_backward: dx = d(loss)/dx and dw = d(loss)/dw (overwritten) from
+ * dH; dw is summed in a fixed order. Its scratch: lce_rmsnorm_workspace_size.
+ * lce_norm_fwd_bwd: norm forward -> lce_fwd_bwd on H -> norm backward in one
+ * call (H, rstd and dH stay in the workspace, lce_workspace_size with
+ * LCE_OP_NORM_FWD_BWD); outputs loss, lse (may be NULL), dx, dw_norm, dW.
+ */
+size_t lce_rmsnorm_workspace_size(int64_t N, int64_t d);
+int lce_rmsnorm_forward(const void* x, const float* w, int64_t N, int64_t d, float eps, void* H, float* rstd,
+                        void* stream);
+int lce_rmsnorm_backward(const void* x, const float* w, const float* rstd, const void* dH, int64_t N, int64_t d,
+                         void* dx, float* dw, void* ws, size_t ws_bytes, void* stream);
+int lce_norm_fwd_bwd(const void* x, const float* w_norm, float eps, const void* W, const int64_t* y, int64_t N,
+                     int64_t d, int64_t V, const float* grad_loss, float* loss, float* lse, void* dx, float* dw_norm,
+                     float* dW, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
 
 /* Synchronise the stream and copy the workspace's device status bits
  * (LCE_DEVICE_*) of the last call that used ws into *flags. */

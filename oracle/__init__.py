@@ -20,7 +20,8 @@ import numpy as np
 from .lce_oracle import (  # noqa: F401
     IGNORE_INDEX, MEAN, SUM, LabelRangeError, decode_bf16, dH_rows_f64,
     dW_rows_f64, forward_rows_f64, grad_scale, lce_bf16, lce_chunked_online,
-    lce_f64, vshard_backward_f64, vshard_merge_f64, vshard_stats_f64,
+    lce_f64, norm_lce_bf16, rmsnorm_backward_f64, rmsnorm_f64, round_bf16_bits,
+    vshard_backward_f64, vshard_merge_f64, vshard_stats_f64,
 )
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

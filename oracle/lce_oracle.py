@@ -302,3 +302,49 @@ def vshard_backward_f64(H, W_shard, y, vocab_offset, lse, scale, *, ignore_index
     p[np.nonzero(here)[0], col[here]] -= 1.0
     G = p * (valid * scale)[:, None]
     return G @ Ws, G.T @ H
+
+
+# ---------------------------------------------------------------------------
+# The final zero-centred RMSNorm in front of the LM head ("XTuner on Ascend
+# 910C: Qwen3.5-2B training optimisation", section 3.1.1: x / rms(x) scaled by
+# (1 + w), one bf16 rounding of the output), and its backward, from the
+# definition.
+# ---------------------------------------------------------------------------
+
+def round_bf16_bits(a) -> np.ndarray:
+    """fp64 -> fp32 -> bf16 bit patterns, round to nearest even."""
+    f = np.ascontiguousarray(np.asarray(a, dtype=np.float64).astype(np.float32))
+    u = f.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def rmsnorm_f64(x, w, eps):
+    """out = x r (1 + w), r_i = 1 / sqrt(mean_k x_ik^2 + eps). Returns (out, r)."""
+    x = np.asarray(x, dtype=np.float64)
+    r = 1.0 / np.sqrt((x * x).mean(axis=1) + eps)
+    return x * r[:, None] * (1.0 + np.asarray(w, dtype=np.float64))[None, :], r
+
+
+def rmsnorm_backward_f64(x, w, r, dout):
+    """dx_ik = r_i ((1 + w_k) dout_ik - x_ik r_i^2 c_i / d), c_i = sum_k dout_ik (1 + w_k) x_ik;
+    dw_k = sum_i dout_ik x_ik r_i."""
+    x = np.asarray(x, dtype=np.float64)
+    g = 1.0 + np.asarray(w, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    r = np.asarray(r, dtype=np.float64)
+    c = (dout * g[None, :] * x).sum(axis=1)
+    dx = r[:, None] * (g[None, :] * dout - x * (r * r * c / x.shape[1])[:, None])
+    dw = (dout * x * r[:, None]).sum(axis=0)
+    return dx, dw
+
+
+def norm_lce_bf16(xbits, w, Wbits, y, eps, **kw):
+    """Norm -> bf16 H -> token cross-entropy -> back through the norm.
+    Returns the lce_f64 dict plus dx, dw_norm (fp64)."""
+    x = decode_bf16(xbits)
+    h, r = rmsnorm_f64(x, w, eps)
+    Hb = decode_bf16(round_bf16_bits(h))
+    out = lce_f64(Hb, decode_bf16(Wbits), y, **kw)
+    out["dx"], out["dw_norm"] = rmsnorm_backward_f64(x, w, r, out["dH"])
+    out["H"] = Hb
+    return out

@@ -383,3 +383,75 @@ def test_vocab_shards_merge_to_the_whole(cuts):
     parts = [oracle.vshard_backward_f64(H, W[a:b], y, a, lse, scale) for a, b in zip(cuts[:-1], cuts[1:])]
     assert _rel(sum(p[0] for p in parts), whole["dH"]) < 1e-13
     assert _rel(np.vstack([p[1] for p in parts]), whole["dW"]) < 1e-13
+
+
+# --------------------------------------------------------------------------
+# The final zero-centred RMSNorm
+# --------------------------------------------------------------------------
+
+def test_rmsnorm_matches_torch_rms_norm_and_autograd():
+    """PyTorch's rms_norm with weight (1 + w), fp64 autograd: out, dx and dw."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(51)
+    x = rng.standard_normal((19, 24)) * 3
+    w = rng.standard_normal(24) * 0.1
+    dout = rng.standard_normal((19, 24))
+    out, r = oracle.rmsnorm_f64(x, w, 1e-6)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    ot = torch.nn.functional.rms_norm(xt, (24,), weight=1.0 + wt, eps=1e-6)
+    ot.backward(torch.tensor(dout))
+    np.testing.assert_allclose(out, ot.detach().numpy(), rtol=1e-13)
+    dx, dw = oracle.rmsnorm_backward_f64(x, w, r, dout)
+    assert _rel(dx, xt.grad.numpy()) < 1e-12
+    assert _rel(dw, wt.grad.numpy()) < 1e-12
+
+
+def test_rmsnorm_closed_form_and_finite_differences():
+    """A constant row c: r = 1/sqrt(c^2 + eps), out = c r (1 + w). Central
+    differences of sum(out * dout) against dx and dw."""
+    w = np.array([0.0, 0.5, -0.25, 1.0])
+    out, r = oracle.rmsnorm_f64(np.full((1, 4), 2.0), w, 1e-6)
+    assert r[0] == pytest.approx(1 / math.sqrt(4 + 1e-6), rel=1e-15)
+    np.testing.assert_allclose(out[0], 2.0 * r[0] * (1 + w), rtol=1e-15)
+    rng = np.random.default_rng(52)
+    x = rng.standard_normal((3, 6))
+    w = rng.standard_normal(6) * 0.2
+    dout = rng.standard_normal((3, 6))
+    f = lambda xx, ww: float((oracle.rmsnorm_f64(xx, ww, 1e-5)[0] * dout).sum())
+    _, r = oracle.rmsnorm_f64(x, w, 1e-5)
+    dx, dw = oracle.rmsnorm_backward_f64(x, w, r, dout)
+    h = 1e-6
+    fdx = np.zeros_like(x)
+    for i in range(3):
+        for k in range(6):
+            xp, xm = x.copy(), x.copy()
+            xp[i, k] += h
+            xm[i, k] -= h
+            fdx[i, k] = (f(xp, w) - f(xm, w)) / (2 * h)
+    fdw = np.array([(f(x, w + h * np.eye(6)[k]) - f(x, w - h * np.eye(6)[k])) / (2 * h) for k in range(6)])
+    assert _rel(dx, fdx) < 1e-8 and _rel(dw, fdw) < 1e-8
+
+
+def test_norm_then_cross_entropy_chain_rule():
+    """Norm + cross-entropy through the oracle equals PyTorch autograd through
+    rms_norm, the bf16 rounding of H treated as the identity for gradients."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(53)
+    N, d, V = 21, 16, 29
+    xb = oracle.round_bf16_bits(rng.standard_normal((N, d)) * 2)
+    Wb = oracle.round_bf16_bits(rng.standard_normal((V, d)) * 0.3)
+    w = rng.standard_normal(d) * 0.1
+    y = rng.integers(0, V, N)
+    y[::5] = -100
+    out = oracle.norm_lce_bf16(xb, w, Wb, y, 1e-6)
+    x = oracle.decode_bf16(xb)
+    xt = torch.tensor(x, requires_grad=True)
+    wt = torch.tensor(w, requires_grad=True)
+    Ht = torch.nn.functional.rms_norm(xt, (d,), weight=1.0 + wt, eps=1e-6)
+    Hq = Ht + (torch.tensor(out["H"]) - Ht).detach()     # forward uses the rounded H
+    L = torch.nn.functional.cross_entropy(Hq @ torch.tensor(oracle.decode_bf16(Wb)).T, torch.tensor(y))
+    L.backward()
+    assert out["loss"] == pytest.approx(L.item(), rel=1e-12)
+    assert _rel(out["dx"], xt.grad.numpy()) < 1e-11
+    assert _rel(out["dw_norm"], wt.grad.numpy()) < 1e-11

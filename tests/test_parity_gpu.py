@@ -218,6 +218,45 @@ def test_vocab_shards_on_one_gpu(cuda_lib, cuts, chunk):
     assert ((lse - lse_full).abs() / lse_full.abs()).max().item() <= TOL_LSE
 
 
+@pytest.mark.parametrize("N,d", [(300, 64), (517, 2048), (130, 7168)])
+def test_rmsnorm_forward_backward(cuda_lib, N, d):
+    torch = _torch()
+    rng = np.random.default_rng(N + d)
+    xb = inputs.f64_to_bf16_bits(rng.standard_normal((N, d)) * 3)
+    w = (rng.standard_normal(d) * 0.1).astype(np.float32)
+    dHb = inputs.f64_to_bf16_bits(rng.standard_normal((N, d)) * 1e-3)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    wt = torch.from_numpy(w).cuda()
+    dH = torch.from_numpy(dHb.view(np.int16)).view(torch.bfloat16).cuda()
+    H, rstd = cuda_lib.lce_rmsnorm_forward(x, wt, 1e-6)
+    dx, dw = cuda_lib.lce_rmsnorm_backward(x, wt, rstd, dH)
+    xo = oracle.decode_bf16(xb)
+    h, r = oracle.rmsnorm_f64(xo, w.astype(np.float64), 1e-6)
+    # one bf16 rounding of an fp32 product: within one bf16 ulp of the exact value
+    assert np.max(np.abs(bf16_to_np(H) - h) / np.maximum(np.abs(h), 1e-30)) <= 2.0 ** -8
+    np.testing.assert_allclose(rstd.cpu().numpy(), r, rtol=1e-5)
+    dx_ref, dw_ref = oracle.rmsnorm_backward_f64(xo, w.astype(np.float64), r, oracle.decode_bf16(dHb))
+    assert rel_fro(bf16_to_np(dx), dx_ref) <= TOL_GRAD
+    assert rel_fro(dw.cpu().numpy(), dw_ref) <= 1e-4
+
+
+def test_norm_fwd_bwd_matches_oracle(cuda_lib):
+    """Norm -> fused linear cross-entropy -> norm backward in one call."""
+    torch = _torch()
+    inp = small_inputs(600, 256, 4096, seed=57, sigma_w=0.05)
+    rng = np.random.default_rng(57)
+    w = (rng.standard_normal(256) * 0.1).astype(np.float32)
+    xb = inputs.f64_to_bf16_bits(rng.standard_normal((600, 256)) * 2)
+    ref = oracle.norm_lce_bf16(xb, w.astype(np.float64), inp["W"], inp["y"], 1e-6)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    _, W, y = to_dev(inp)
+    loss, lse, dx, dw_norm, dW = cuda_lib.lce_norm_fwd_bwd(x, torch.from_numpy(w).cuda(), W, y, chunk_tokens=256,
+                                                           sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), None, dW.cpu().numpy())
+    assert rel_fro(bf16_to_np(dx), ref["dx"]) <= TOL_GRAD
+    assert rel_fro(dw_norm.cpu().numpy(), ref["dw_norm"]) <= TOL_GRAD
+
+
 def test_all_ignored_and_empty(cuda_lib):
     torch = _torch()
     inp = small_inputs(130, 64, 600, seed=3)
