@@ -1,9 +1,11 @@
 """Parity of the CUDA path (through the C ABI) with the fp64 CPU oracle.
 
-Tolerances (written here, derived in the design doc):
-  loss: relative error <= 1e-3;  dH, dW: relative Frobenius error <= 5e-3;
+Tolerances:
+  loss: relative error <= 1e-3;  dH, dW: relative Frobenius error <= 5e-3
+  (the gradient tile and dH are rounded to bf16: about 1.6e-3 rms relative
+  each, so 5e-3 leaves room for both);
   lse: max relative error <= 1e-4 (fp32 logits and sum-exp; the fp64 oracle
-  differs only by fp32 accumulation and exp rounding, ~1e-6);
+  differs only by fp32 accumulation and exp rounding, ~1e-7 measured);
   the softmax-only rows of dW (vocabulary rows no valid label hits) are also
   held to 5e-3 on their own, because in the full dW the one-hot rows dominate
   the norm and would hide an error in the softmax part.
