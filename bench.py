@@ -318,7 +318,7 @@ def main():
     flops_step = 6.0 * N * V * d
     tflops = flops_step * args.steps / (ms * 1e-3) / 1e12
     # dominant kernel of the timed region
-    gemm_kinds = {"logits_stats", "logits_grad", "gemm_dH", "gemm_dW"}
+    gemm_kinds = set(lce.GEMM_KINDS)
     dom = max(prof, key=lambda k: prof[k]["ms"])
     p = prof[dom]
     per_launch_ms = p["ms"] / max(1, p["launches"])

@@ -749,6 +749,18 @@ int lce_norm_fwd_bwd(const void* x, const float* w_norm, float eps, const void* 
   return LCE_OK;
 }
 
+int lce_scale_grads(void* dH, float* dW, int64_t N, int64_t d, int64_t V, const float* grad_loss, void* stream) {
+  if (N < 0 || d <= 0 || d % 8 != 0 || V < 0 || !grad_loss) return LCE_ERR_INVALID_ARG;
+  if ((dH && !aligned(dH, 16)) || (dW && !aligned(dW, 16)) || !aligned(grad_loss, 4)) return LCE_ERR_ALIGNMENT;
+  DeviceInfo dev;
+  LCE_TRY(device_check(&dev));
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long nbf = dH ? N * d : 0, nf = dW ? V * d : 0;
+  return timed(s, K_OTHER, 4.0 * static_cast<double>(nbf) + 8.0 * static_cast<double>(nf), [&] {
+    return cuda_rc(lce::launch_scale(dH, nbf, dW, nf, grad_loss, dev.num_sms, s));
+  });
+}
+
 int lce_read_device_status(const void* ws, void* stream, int* flags) {
   if (!ws || !flags) return LCE_ERR_INVALID_ARG;
   if (!aligned(ws, 256)) return LCE_ERR_ALIGNMENT;

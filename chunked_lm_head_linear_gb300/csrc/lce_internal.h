@@ -113,6 +113,9 @@ cudaError_t launch_rmsnorm_fwd(const void* x, const float* w, long long N, int d
                                cudaStream_t s);
 cudaError_t launch_rmsnorm_bwd(const void* x, const float* w, const float* rstd, const void* dH, long long N, int d,
                                void* dx, float* dw, float* part, cudaStream_t s);
+// In-place x *= *g of n_bf16 bf16 values (a multiple of 8) and n_f32 fp32 values (a multiple of 4).
+cudaError_t launch_scale(void* bf16, long long n_bf16, float* f32, long long n_f32, const float* g, int num_sms,
+                         cudaStream_t s);
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s);
 
 // GEMM tile geometry (must match the kernels): each CTA of a pair loads 128

@@ -437,6 +437,32 @@ __global__ void __launch_bounds__(256) k_shard_merge(const float4* __restrict__ 
   loss_i[i] = valid ? l - zt : 0.f;
 }
 
+// x *= g in place for bf16 (8 per thread) and fp32 (4 per thread) arrays;
+// nothing is read or written when g == 1.
+__global__ void __launch_bounds__(256) k_scale(uint4* __restrict__ bf, long long nbf8, float4* __restrict__ f32,
+                                               long long nf4, const float* __restrict__ gptr) {
+  const float g = *gptr;
+  if (g == 1.f) return;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nbf8; i += stride) {
+    const uint4 v = bf[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * g, __uint_as_float(w[q] & 0xffff0000u) * g);
+    bf[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < nf4; i += stride) {
+    float4 v = f32[i];
+    v.x *= g;
+    v.y *= g;
+    v.z *= g;
+    v.w *= g;
+    f32[i] = v;
+  }
+}
+
 // loss = (sum_i loss_i) * lscale, fp64 accumulation in a fixed order.
 __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ loss_i, long long N,
                                                    const DevStatus* st, float* loss) {
@@ -721,6 +747,14 @@ cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const in
   if (N <= 0) return cudaSuccess;
   const long long grid = (N + 255) / 256;
   k_shard_merge<<<static_cast<unsigned>(grid), 256, 0, s>>>(stats, R, N, y, V_total, ignore_index, lse, loss_i);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale(void* bf16, long long n_bf16, float* f32, long long n_f32, const float* g, int num_sms,
+                         cudaStream_t s) {
+  if (n_bf16 <= 0 && n_f32 <= 0) return cudaSuccess;
+  k_scale<<<num_sms * 4, 256, 0, s>>>(static_cast<uint4*>(bf16), n_bf16 / 8, reinterpret_cast<float4*>(f32),
+                                      n_f32 / 4, g);
   return cudaGetLastError();
 }
 

@@ -38,8 +38,11 @@ EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward"
             "lce_read_device_status", "lce_status_string", "lce_version", "lce_profile_begin",
             "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk",
             "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward",
-            "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd")
+            "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd",
+            "lce_scale_grads")
 LCE_KERNEL_KINDS = 10
+# Kernel kinds whose profiled work is flops (tensor-core GEMMs); the others count bytes.
+GEMM_KINDS = ("logits_stats", "logits_grad", "gemm_dH_dW", "logits_ref")
 
 
 class LceOpts(ctypes.Structure):
@@ -112,6 +115,8 @@ def load(path: str | None = None):
         lib.lce_rmsnorm_backward.restype = I32
         lib.lce_norm_fwd_bwd.argtypes = [P, P, F32, P, P, I64, I64, I64, P, P, P, P, P, P, OPT, P, ctypes.c_size_t, P]
         lib.lce_norm_fwd_bwd.restype = I32
+        lib.lce_scale_grads.argtypes = [P, P, I64, I64, I64, P, P]
+        lib.lce_scale_grads.restype = I32
         lib.lce_auto_chunk.argtypes = [I64, I64, I64, ctypes.c_size_t, OPT]
         lib.lce_auto_chunk.restype = I64
         lib.lce_forward_noalloc.argtypes = [P, P, P, I64, I64, I64, P, P, OPT, P]
@@ -389,3 +394,10 @@ def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, work
                                  _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_norm_fwd_bwd")
     return loss, lse, dx, dw_norm, dW
+
+
+def lce_scale_grads(dH, dW, grad_loss, *, stream=None):
+    """In place: dH *= g, dW *= g with g = grad_loss[0] read on the device (no-op when g == 1)."""
+    N, d = (dH.shape if dH is not None else (0, dW.shape[1]))
+    V = dW.shape[0] if dW is not None else 0
+    _raise(load().lce_scale_grads(_ptr(dH), _ptr(dW), N, d, V, _ptr(grad_loss), _stream(stream)), "lce_scale_grads")

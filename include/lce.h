@@ -207,6 +207,14 @@ int lce_norm_fwd_bwd(const void* x, const float* w_norm, float eps, const void* 
                      int64_t d, int64_t V, const float* grad_loss, float* loss, float* lse, void* dx, float* dw_norm,
                      float* dW, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
 
+/* Scale gradients computed for an upstream gradient of 1 by the actual one,
+ * in place: dH [N, d] bf16 and dW [V, d] fp32 (either may be NULL) times
+ * *grad_loss (device fp32). When *grad_loss == 1 the kernel returns without
+ * touching memory. For frameworks whose loss node computes the gradients in
+ * its forward pass (as the fused Liger loss does) and receives the upstream
+ * gradient only in its backward. No host synchronisation. */
+int lce_scale_grads(void* dH, float* dW, int64_t N, int64_t d, int64_t V, const float* grad_loss, void* stream);
+
 /* Synchronise the stream and copy the workspace's device status bits
  * (LCE_DEVICE_*) of the last call that used ws into *flags. */
 int lce_read_device_status(const void* ws, void* stream, int* flags);

@@ -155,3 +155,10 @@ def test_auto_chunk_policy(lib):
                                       lce.make_opts(chunk_tokens=C + 256)) > budget
     assert lce.auto_chunk(65536, 4096, V, 1 << 20) == 0          # nothing fits in 1 MiB
     assert lce.auto_chunk(8192, 7, V, big) == 0                  # invalid d
+
+
+def test_profiler_kind_names(lib):
+    names = [lib.lce_kernel_name(k).decode() for k in range(lce.LCE_KERNEL_KINDS)]
+    assert len(set(names)) == lce.LCE_KERNEL_KINDS
+    assert set(lce.GEMM_KINDS) <= set(names)
+    assert lib.lce_kernel_name(lce.LCE_KERNEL_KINDS) is None

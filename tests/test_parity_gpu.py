@@ -259,6 +259,25 @@ def test_norm_fwd_bwd_matches_oracle(cuda_lib):
     assert rel_fro(dw_norm.cpu().numpy(), ref["dw_norm"]) <= TOL_GRAD
 
 
+@pytest.mark.parametrize("recompute", [False, True])
+def test_autograd_wrapper(cuda_lib, recompute):
+    """loss.backward() through the torch.autograd wrapper, with an upstream
+    gradient of 1 and of 2.5 (the loss scaled before backward)."""
+    torch = _torch()
+    from chunked_lm_head_linear_gb300.autograd import FusedLinearCrossEntropy
+    inp = small_inputs(400, 128, 3000, seed=61)
+    for scale in (1.0, 2.5):
+        ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"], grad_loss=scale)
+        H, W, y = to_dev(inp)
+        H.requires_grad_(True)
+        W.requires_grad_(True)
+        loss = FusedLinearCrossEntropy(recompute=recompute, chunk_tokens=128)(H, W, y)
+        (loss * scale).backward()
+        assert abs(loss.item() - ref["loss"]) <= TOL_LOSS * ref["loss"]
+        assert rel_fro(bf16_to_np(H.grad), ref["dH"]) <= TOL_GRAD
+        assert rel_fro(W.grad.float().cpu().numpy(), ref["dW"]) <= TOL_GRAD
+
+
 def test_all_ignored_and_empty(cuda_lib):
     torch = _torch()
     inp = small_inputs(130, 64, 600, seed=3)
