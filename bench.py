@@ -185,10 +185,17 @@ def run_reference(args, w):
 
 
 def config_of(w, chunk, args):
-    return {"workload": w.name, "N_tokens_per_gpu": w.N, "d": w.d, "V": w.V, "chunk_tokens": chunk,
+    cfg = {"workload": w.name, "N_tokens_per_gpu": w.N, "d": w.d, "V": w.V, "chunk_tokens": chunk,
             "labels": w.labels, "ignore": w.ignore, "seed": w.seed,
             "global_batch_tokens": w.N * args.gpus, "parallelism": f"dp{args.gpus}",
             "l2": "inputs larger than L2 (W 0.62 GB, dW 1.24 GB, gradient tiles > 1 GB); no flush"}
+    if getattr(args, "slices", 0) > 0:
+        cfg["dw_slices"] = args.slices
+        cfg["sm_limit"] = args.sm_limit
+        if args.gpus > 1:
+            cfg["parallelism"] = f"fsdp{args.gpus} (dW reduced to vocabulary-row owners)"
+            cfg["weight_gather"] = "outside the step (FSDP gathers it while the layer before computes)"
+    return cfg
 
 
 # ---------------------------------------------------------------------------
@@ -205,6 +212,10 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the workload's token count (same d, V and label law); for small profiling runs")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--slices", type=int, default=0,
+                    help="finish dW in this many vocabulary slices (lce_fwd_bwd_sliced); with --gpus > 1 the "
+                         "FSDP-style step: dW reduced to its row owners slice by slice on a side stream")
+    ap.add_argument("--sm-limit", type=int, default=0, help="with --slices: SMs the GEMM launches may use (0 = all)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -220,7 +231,7 @@ def main():
 
     import torch
     import torch.distributed as dist
-    from chunked_lm_head_linear_gb300 import dp, lce
+    from chunked_lm_head_linear_gb300 import dp, fsdp, lce
 
     torch.cuda.set_device(local)
     if world > 1:
@@ -246,8 +257,20 @@ def main():
     lse = torch.empty(N, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
 
+    bounds = lce.slice_bounds(V, args.slices) if args.slices > 0 else None
+    owners = fsdp.owner_bounds(V, world)
+    slice_events = [torch.cuda.Event() for _ in range(len(bounds) - 1)] if bounds else None
+    comm = torch.cuda.Stream(dev) if (bounds and world > 1) else None
+
     def step(Hx, yx):
-        if world > 1:
+        if bounds and world > 1:
+            loss, _, dH, _ = fsdp.fsdp_fwd_bwd(Hx, W, yx, owners=owners, slices=bounds, comm_stream=comm,
+                                               sm_limit=args.sm_limit, dW=dW, lse=lse, workspace=ws,
+                                               chunk_tokens=chunk)
+        elif bounds:
+            loss, _, dH, _ = lce.lce_fwd_bwd_sliced(Hx, W, yx, bounds=bounds, events=slice_events,
+                                                    sm_limit=args.sm_limit, dW=dW, lse=lse, workspace=ws, **opts)
+        elif world > 1:
             loss, _, dH, _ = dp.dp_fwd_bwd(Hx, W, yx, n_global=n_global, dW=dW, lse=lse, workspace=ws,
                                            chunk_tokens=chunk)
         else:

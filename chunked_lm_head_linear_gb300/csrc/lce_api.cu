@@ -341,10 +341,17 @@ int forward_chunk(const Call& c, int64_t c0, int64_t rows, float* lse, float* lo
   });
 }
 
+// Which part of the backward one launch computes: the dW rows [v_begin, v_end)
+// (v_end < 0: to V) and, if with_dh, the chunk's dH.
+struct BwdPart {
+  int64_t v_begin = 0, v_end = -1;
+  bool with_dh = true;
+};
+
 // dH_c = (g/n) [rowscale] (G W) and dW (+)= (g/n) G^T B, with G [rows, V] in
 // the chunk's tile buffer and B = H_c or Ht: one launch for both GEMMs.
 int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, void* dH, float* dW,
-          bool accumulate, bool dH_f32 = false) {
+          bool accumulate, bool dH_f32 = false, const BwdPart& part = BwdPart()) {
   const uint16_t* P = reinterpret_cast<const uint16_t*>(c.ws + c.L.P);
   CUtensorMap mG, mW, mdH, mGt, mB, mdW;
   LCE_TRY(make_map(&mG, P, rows, c.V, c.L.ldp, lce::kBoxRowsK));      // dH: A, K-major
@@ -372,11 +379,44 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   wp.ld = c.d;
   wp.accumulate = accumulate ? 1 : 0;
   wp.st = c.st;
-  const double flops = 4.0 * static_cast<double>(rows) * static_cast<double>(c.V) * static_cast<double>(c.d);
+  const int64_t v_end = part.v_end < 0 ? c.V : part.v_end;
+  const double dw_rows = static_cast<double>(v_end - part.v_begin);
+  const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(c.d) *
+                       ((part.with_dh ? static_cast<double>(c.V) : 0.0) + dw_rows);
   return timed(c.s, K_GEMM_BWD, flops, [&] {
     return cuda_rc(lce::launch_backward(mG, mW, mdH, mGt, mB, mdW, rows, c.V, c.d, dp, wp, &c.st->flags,
-                                        c.dev.num_sms, c.s));
+                                        c.dev.num_sms, c.s, part.v_begin, v_end, part.with_dh));
   });
+}
+
+// dW in vocabulary slices (lce_fwd_bwd_sliced): the last chunk's backward runs
+// as one launch per slice, the dH tiles with the last slice, and events[s] is
+// recorded once rows [bounds[s], bounds[s+1]) of dW are final.
+struct Slices {
+  int n = 0;
+  const int64_t* bounds = nullptr;
+  void* const* events = nullptr;
+};
+
+int record_slice_events(const Call& c, const Slices* sl, int first) {
+  if (!sl || !sl->events) return LCE_OK;
+  for (int k = first; k < sl->n; ++k)
+    LCE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(sl->events[k]), c.s));
+  return LCE_OK;
+}
+
+int dh_dw_sliced(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const uint16_t* B, void* dH,
+                 float* dW, bool accumulate, const Slices& sl) {
+  for (int k = 0; k < sl.n; ++k) {
+    BwdPart part;
+    part.v_begin = sl.bounds[k];
+    part.v_end = sl.bounds[k + 1];
+    part.with_dh = k == sl.n - 1;
+    if (part.with_dh || part.v_end > part.v_begin)
+      LCE_TRY(dh_dw(c, c0, rows, rowscale, B, dH, dW, accumulate, false, part));
+    if (sl.events) LCE_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(sl.events[k]), c.s));
+  }
+  return LCE_OK;
 }
 
 // Backward of one chunk from a known lse: recompute the logits into the
@@ -394,7 +434,7 @@ int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, vo
 // Forward and backward of one chunk without recomputing the logits: the
 // forward stores the exp tile, the backward rescales it per row.
 int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* lse, float* loss_i, uint16_t* dH,
-                float* dW, bool accumulate) {
+                float* dW, bool accumulate, const Slices* sl = nullptr) {
   uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
   float* ref = reinterpret_cast<float*>(c.ws + c.L.ref);
   float* alpha = reinterpret_cast<float*>(c.ws + c.L.alpha);
@@ -433,6 +473,7 @@ int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* l
                                       static_cast<int>(rows), static_cast<int>(c.d),
                                       reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
   }));
+  if (sl) return dh_dw_sliced(c, c0, rows, alpha, Ht, dH, dW, accumulate, *sl);
   return dh_dw(c, c0, rows, alpha, Ht, dH, dW, accumulate);
 }
 
@@ -559,9 +600,13 @@ int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int6
   return finish(c);
 }
 
-int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
-                const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts, void* ws,
-                size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V, const float* grad_loss,
+            float* loss, float* lse, void* dH, float* dW, const lce_opts* opts, void* ws, size_t ws_bytes,
+            void* stream, const Slices* sl, int sm_limit) {
   Call c;
   LCE_TRY(begin(&c, LCE_OP_FWD_BWD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
   if (c.o.reserved != 0) return LCE_ERR_INVALID_ARG;
@@ -570,19 +615,51 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
       (grad_loss && !aligned(grad_loss, 4)))
     return LCE_ERR_ALIGNMENT;
   LCE_TRY(device_check(&c.dev));
+  if (sm_limit > 0 && sm_limit < c.dev.num_sms) c.dev.num_sms = sm_limit & ~1;
   float* lse_rows = lse ? lse : reinterpret_cast<float*>(c.ws + c.L.lse);
   float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
   LCE_TRY(prepare(c, grad_loss));
   if (N == 0 && !c.o.accumulate_dW)
     LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
                   [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
+  if (N == 0) LCE_TRY(record_slice_events(c, sl, 0));
   for (int64_t k = 0, c0 = 0; c0 < N; ++k, c0 += c.L.C) {
     const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
+    const bool last = c0 + rows >= N;
     LCE_TRY(fused_chunk(c, k, c0, rows, lse_rows, loss_i, static_cast<uint16_t*>(dH), dW,
-                        c.o.accumulate_dW || c0 > 0));
+                        c.o.accumulate_dW || c0 > 0, last ? sl : nullptr));
   }
   LCE_TRY(finalize(c, loss_i, loss));
   return finish(c);
+}
+
+}  // namespace
+
+extern "C" {
+
+int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts, void* ws,
+                size_t ws_bytes, void* stream) {
+  return fwd_bwd(H, W, y, N, d, V, grad_loss, loss, lse, dH, dW, opts, ws, ws_bytes, stream, nullptr, 0);
+}
+
+int lce_fwd_bwd_sliced(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                       const float* grad_loss, float* loss, float* lse, void* dH, float* dW, int32_t n_slices,
+                       const int64_t* slice_bounds, void* const* slice_events, int32_t sm_limit,
+                       const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  if (n_slices < 1 || n_slices > LCE_MAX_SLICES || !slice_bounds || sm_limit < 0 || sm_limit == 1)
+    return LCE_ERR_INVALID_ARG;
+  if (slice_bounds[0] != 0 || slice_bounds[n_slices] != V) return LCE_ERR_INVALID_ARG;
+  for (int k = 0; k < n_slices; ++k) {
+    if (slice_bounds[k + 1] < slice_bounds[k]) return LCE_ERR_INVALID_ARG;
+    if (k > 0 && slice_bounds[k] % LCE_SLICE_ALIGN != 0) return LCE_ERR_INVALID_ARG;
+    if (slice_events && !slice_events[k]) return LCE_ERR_INVALID_ARG;
+  }
+  Slices sl;
+  sl.n = n_slices;
+  sl.bounds = slice_bounds;
+  sl.events = slice_events;
+  return fwd_bwd(H, W, y, N, d, V, grad_loss, loss, lse, dH, dW, opts, ws, ws_bytes, stream, &sl, sm_limit);
 }
 
 static int shard_args(int64_t V_shard, int64_t vocab_offset, int64_t V_total) {

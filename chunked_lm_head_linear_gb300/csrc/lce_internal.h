@@ -88,10 +88,13 @@ cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUte
                           long long K, const FwdParams& ep, int no_loads, int num_sms, cudaStream_t s);
 // Backward GEMMs of a chunk in one launch: dH_c = G W (ah: G K-major, bh: W
 // N-major, ch: dH store) and dW (+)= G^T B (aw: G M-major, bw: B N-major, cw:
-// dW store / reduce-add).
+// dW store / reduce-add). Only the dW rows [v_begin, v_end) are computed
+// (v_end < 0: to V; v_begin a multiple of 256), and the dH tiles only if
+// with_dh; every tile computed is the same as in the whole launch.
 cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
                             const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
-                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s);
+                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s,
+                            long long v_begin = 0, long long v_end = -1, bool with_dh = true);
 cudaError_t launch_combine(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,

@@ -553,6 +553,7 @@ struct BwdProb {
     CUtensorMap ah, bh, ch, aw, bw, cw;
     int h_m, h_n, h_k;   // dH: 256-row blocks of the chunk, 256-column blocks of d, k-blocks of V
     int w_m, w_n, w_k;   // dW: 256-row blocks of V, 256-column blocks of d, k-blocks of the chunk
+    int w_t0, w_tiles;   // this launch's dW tiles: [w_t0, w_t0 + w_tiles) in (row block, column block) order
     int w_phase1;        // dW tiles dealt round-robin to every cluster (a multiple of the cluster count)
     int* flags;
     DhParams h;
@@ -567,7 +568,7 @@ struct BwdProb {
   };
   static __device__ __forceinline__ Sched sched(const Params& p, int c, int P) {
     Sched s;
-    const int nH = p.h_m * p.h_n, nW = p.w_m * p.w_n;
+    const int nH = p.h_m * p.h_n, nW = p.w_tiles;
     s.hcount = c < nH ? (nH - 1 - c) / P + 1 : 0;
     const int r = nH % P;  // clusters c < r hold one dH tile more
     s.q1 = p.w_phase1 / P;
@@ -587,7 +588,7 @@ struct BwdProb {
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const Sched s = sched(p, c, P);
     if (j < s.q1) {
-      const int t = c + j * P;
+      const int t = p.w_t0 + c + j * P;
       return TileJob{KIND_DW, t / p.w_n, t % p.w_n, p.w_k};
     }
     j -= s.q1;
@@ -596,7 +597,7 @@ struct BwdProb {
       return TileJob{KIND_DH, t / p.h_n, t % p.h_n, p.h_k};
     }
     j -= s.hcount;
-    const int t = p.w_phase1 + s.li + j * s.nlight;
+    const int t = p.w_t0 + p.w_phase1 + s.li + j * s.nlight;
     return TileJob{KIND_DW, t / p.w_n, t % p.w_n, p.w_k};
   }
   static __device__ __forceinline__ void load(const Params& p, int kind, uint8_t* a, uint8_t* b, uint32_t bar,
@@ -664,7 +665,8 @@ cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUte
 
 cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
                             const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
-                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s) {
+                            const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s,
+                            long long v_begin, long long v_end, bool with_dh) {
   BwdProb::Params p;
   p.ah = ah;
   p.bh = bh;
@@ -672,16 +674,23 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   p.aw = aw;
   p.bw = bw;
   p.cw = cw;
-  p.h_m = ceil_div_i(rows, P_TILE_M);
+  p.h_m = with_dh ? ceil_div_i(rows, P_TILE_M) : 0;
   p.h_n = ceil_div_i(d, BN);
   p.h_k = ceil_div_i(V, BK);
   p.w_m = ceil_div_i(V, P_TILE_M);
   p.w_n = ceil_div_i(d, BN);
   p.w_k = ceil_div_i(rows, BK);
+  // dW tiles of the vocabulary rows [v_begin, v_end) (v_begin a multiple of the tile height)
+  if (v_end < 0 || v_end > V) v_end = V;
+  if (v_begin < 0) v_begin = 0;
+  const int vb0 = static_cast<int>(v_begin / P_TILE_M);
+  const int vb1 = v_end > v_begin ? ceil_div_i(v_end, P_TILE_M) : vb0;
+  p.w_t0 = vb0 * p.w_n;
+  p.w_tiles = (vb1 - vb0) * p.w_n;
   p.flags = flags;
   p.h = h;
   p.w = w;
-  const long long nH = static_cast<long long>(p.h_m) * p.h_n, nW = static_cast<long long>(p.w_m) * p.w_n;
+  const long long nH = static_cast<long long>(p.h_m) * p.h_n, nW = p.w_tiles;
   const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
   if (P <= 0) return cudaSuccess;
   // Balance: every cluster should end with ~(nH h_k + nW w_k) / P k-blocks.

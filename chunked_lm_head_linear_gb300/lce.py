@@ -39,7 +39,7 @@ EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward"
             "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk",
             "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward",
             "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd",
-            "lce_scale_grads")
+            "lce_scale_grads", "lce_fwd_bwd_sliced")
 LCE_KERNEL_KINDS = 10
 # Kernel kinds whose profiled work is flops (tensor-core GEMMs); the others count bytes.
 GEMM_KINDS = ("logits_stats", "logits_grad", "gemm_dH_dW", "logits_ref")
@@ -89,6 +89,9 @@ def load(path: str | None = None):
         lib.lce_backward.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, OPT, P, ctypes.c_size_t, P]
         lib.lce_backward.restype = I32
         lib.lce_fwd_bwd.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, P, OPT, P, ctypes.c_size_t, P]
+        lib.lce_fwd_bwd_sliced.restype = I32
+        lib.lce_fwd_bwd_sliced.argtypes = [P, P, P, I64, I64, I64, P, P, P, P, P, I32, ctypes.POINTER(I64),
+                                           ctypes.POINTER(P), I32, OPT, P, ctypes.c_size_t, P]
         lib.lce_fwd_bwd.restype = I32
         lib.lce_read_device_status.argtypes = [P, P, ctypes.POINTER(I32)]
         lib.lce_read_device_status.restype = I32
@@ -256,6 +259,58 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
     rc = load().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(dH),
                             _ptr(dW), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_fwd_bwd")
+    return loss, lse, dH, dW
+
+
+LCE_MAX_SLICES = 4096
+LCE_SLICE_ALIGN = 256
+
+
+def slice_bounds(V: int, n_slices: int) -> list:
+    """Vocabulary cut into n_slices contiguous row ranges of (nearly) equal
+    numbers of 256-row dW tiles: [0, b_1, ..., V], interior bounds multiples of 256."""
+    if n_slices < 1:
+        raise ValueError("n_slices must be >= 1")
+    tiles = (V + LCE_SLICE_ALIGN - 1) // LCE_SLICE_ALIGN
+    n = min(n_slices, max(tiles, 1))
+    b = [min(V, LCE_SLICE_ALIGN * ((k * tiles) // n)) for k in range(n + 1)]
+    b[-1] = V
+    return b
+
+
+def lce_fwd_bwd_sliced(H, W, y, grad_loss=None, *, bounds, events=None, sm_limit: int = 0, dW=None, lse=None,
+                       workspace=None, stream=None, **opt_kw):
+    """lce_fwd_bwd whose dW is finished slice by slice: ``events[s]`` (torch.cuda.Event,
+    or None for no events) is recorded on the stream once dW rows
+    [bounds[s], bounds[s+1]) are final. Same outputs as lce_fwd_bwd, bit for bit."""
+    import torch
+    N, d, V = _check_inputs(H, W, y)
+    if "chunk_tokens" in opt_kw:
+        opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
+    opts = make_opts(**opt_kw)
+    n = len(bounds) - 1
+    if n < 1:
+        raise ValueError("bounds must hold at least two entries")
+    ws = _workspace(LCE_OP_FWD_BWD, N, d, V, opts, H.device, workspace)
+    loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    if lse is None:
+        lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
+    dH = torch.empty_like(H)
+    if dW is None:
+        dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
+    b = (ctypes.c_int64 * (n + 1))(*[int(x) for x in bounds])
+    ev = None
+    if events is not None:
+        if len(events) != n:
+            raise ValueError("one event per slice")
+        st = stream if stream is not None else torch.cuda.current_stream(H.device)
+        for e in events:          # creates the underlying CUDA event if it does not exist yet
+            e.record(st)
+        ev = (ctypes.c_void_p * n)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    rc = load().lce_fwd_bwd_sliced(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss), _ptr(loss), _ptr(lse),
+                                   _ptr(dH), _ptr(dW), n, b, ev, int(sm_limit), ctypes.byref(opts), _ptr(ws),
+                                   ws.numel(), _stream(stream))
+    _raise(rc, "lce_fwd_bwd_sliced")
     return loss, lse, dH, dW
 
 

@@ -133,6 +133,41 @@ int lce_fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64
                 const float* grad_loss, float* loss, float* lse, void* dH, float* dW, const lce_opts* opts,
                 void* ws, size_t ws_bytes, void* stream);
 
+/* lce_fwd_bwd with dW finished in vocabulary slices, so that its reduction
+ * over data-parallel ranks (FSDP's reduce-scatter of the weight gradient)
+ * can run on another stream while the backward is still computing. FSDP
+ * shards every parameter evenly over the ranks and hides its communication
+ * behind computation ("XTuner V1 introduction", communication masking
+ * section; "XTuner on Ascend 910C: Qwen3.5-2B training optimisation",
+ * section 3.2.1, for the gather of the parameters); the gradient reduction
+ * is the mirror step of the backward.
+ *
+ * Same arguments and workspace as lce_fwd_bwd (LCE_OP_FWD_BWD) plus:
+ *   n_slices      1 .. LCE_MAX_SLICES
+ *   slice_bounds  host int64 [n_slices + 1]: 0 = b_0 <= b_1 <= ... <= b_n = V;
+ *                 every interior bound a multiple of LCE_SLICE_ALIGN (the dW
+ *                 tile height). Slice s is dW rows [b_s, b_{s+1}).
+ *   slice_events  host array of n_slices cudaEvent_t (as void*), created by
+ *                 the caller, or NULL. events[s] is recorded on the stream
+ *                 right after the last launch that writes slice s; a
+ *                 cudaStreamWaitEvent on it orders later work (a collective
+ *                 on another stream) after the final values of that slice.
+ *                 All events are recorded before this call returns.
+ *   sm_limit      0 = all SMs; else the CTA-pair GEMM launches of this call
+ *                 use at most sm_limit SMs (rounded down to even, >= 2), so
+ *                 that kernels on other streams (collectives) find free SMs.
+ * The last chunk's backward runs as n_slices launches in slice order: dW
+ * rows of slices 0 .. n-2 alone, then slice n-1 together with the chunk's
+ * dH. Earlier chunks are unchanged. Every output (loss, lse, dH, dW) is
+ * bitwise identical to lce_fwd_bwd's: each output tile is computed by the
+ * same arithmetic, whichever launch it falls in. */
+#define LCE_MAX_SLICES 4096
+#define LCE_SLICE_ALIGN 256
+int lce_fwd_bwd_sliced(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d, int64_t V,
+                       const float* grad_loss, float* loss, float* lse, void* dH, float* dW, int32_t n_slices,
+                       const int64_t* slice_bounds, void* const* slice_events, int32_t sm_limit,
+                       const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
+
 /* Forward that allocates nothing and takes no workspace, for callers that
  * cannot allocate device memory: their memory is wholly owned by another
  * allocator (a framework's caching pool or a runtime's arena), or they must

@@ -162,3 +162,42 @@ def test_profiler_kind_names(lib):
     assert len(set(names)) == lce.LCE_KERNEL_KINDS
     assert set(lce.GEMM_KINDS) <= set(names)
     assert lib.lce_kernel_name(lce.LCE_KERNEL_KINDS) is None
+
+
+def test_sliced_bounds_checked_on_host(lib):
+    o = lce.make_opts()
+    P = FAKE
+
+    def call(bounds, n=None, events=None, sm=0, V=1000):
+        n = len(bounds) - 1 if n is None else n
+        b = (ctypes.c_int64 * len(bounds))(*bounds)
+        return lib.lce_fwd_bwd_sliced(P, P, P, 64, 64, V, None, P, P, P, P, n, b, events, sm,
+                                      ctypes.byref(o), P, 1 << 40, None)
+
+    E = lce
+    assert call([0, 100, 1000]) == E.LCE_ERR_INVALID_ARG          # interior bound not a multiple of 256
+    assert call([0, 512, 256, 1000]) == E.LCE_ERR_INVALID_ARG     # decreasing
+    assert call([1, 1000]) == E.LCE_ERR_INVALID_ARG               # does not start at 0
+    assert call([0, 999]) == E.LCE_ERR_INVALID_ARG                # does not end at V
+    assert call([0, 1000], n=0) == E.LCE_ERR_INVALID_ARG
+    assert call([0] * (lce.LCE_MAX_SLICES + 1) + [1000], n=lce.LCE_MAX_SLICES + 1) == E.LCE_ERR_INVALID_ARG
+    assert call([0, 1000], sm=1) == E.LCE_ERR_INVALID_ARG
+    assert call([0, 1000], sm=-2) == E.LCE_ERR_INVALID_ARG
+    null_ev = (ctypes.c_void_p * 2)(None, None)
+    assert call([0, 256, 1000], events=null_ev) == E.LCE_ERR_INVALID_ARG
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():      # valid bounds get as far as the device check
+        assert call([0, 0, 256, 1000]) in (E.LCE_ERR_CUDA, E.LCE_ERR_UNSUPPORTED_DEVICE)
+
+
+def test_slice_bounds_helper():
+    b = lce.slice_bounds(151936, 8)
+    assert b[0] == 0 and b[-1] == 151936 and len(b) == 9
+    assert all(x % lce.LCE_SLICE_ALIGN == 0 for x in b[1:-1])
+    assert all(b[k] < b[k + 1] for k in range(8))
+    tiles = [(b[k + 1] - b[k] + 255) // 256 for k in range(8)]
+    assert max(tiles) - min(tiles) <= 1
+    assert lce.slice_bounds(1000, 1) == [0, 1000]
+    assert lce.slice_bounds(300, 5) == [0, 256, 300]            # no more slices than dW tiles
+    with pytest.raises(ValueError):
+        lce.slice_bounds(1000, 0)
