@@ -19,8 +19,8 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblce.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
-          "-I" + os.path.join(ROOT, "include")]
+CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
+INCLUDE = ["-I" + os.path.join(ROOT, "include")]
 SOURCES = ["lce_kernels.cu", "lce_api.cu", "lce_noalloc.cu", "lce_rmsnorm.cu"]
 
 
@@ -39,7 +39,7 @@ def _stamp(extra=()) -> str:
             h.update(name.encode())
             with open(p, "rb") as f:
                 h.update(f.read())
-    h.update(" ".join(ARCH + CFLAGS + list(extra)).encode())
+    h.update(" ".join(ARCH + CFLAGS + list(extra)).encode())  # not the checkout's path: same stamp anywhere
     return h.hexdigest()
 
 
@@ -62,7 +62,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     for src in SOURCES:
         obj = os.path.join(BUILD, src.replace(".cu", ".o"))
         objs.append(obj)
-        cmd = [cc, *ARCH, *CFLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [cc, *ARCH, *CFLAGS, *INCLUDE, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
