@@ -189,6 +189,13 @@ def config_of(w, chunk, args):
             "labels": w.labels, "ignore": w.ignore, "seed": w.seed,
             "global_batch_tokens": w.N * args.gpus, "parallelism": f"dp{args.gpus}",
             "l2": "inputs larger than L2 (W 0.62 GB, dW 1.24 GB, gradient tiles > 1 GB); no flush"}
+    if getattr(args, "path", "fused") != "fused":
+        cfg["path"] = args.path
+        if args.path == "vshard":
+            cfg["vocab_shards"] = args.shards
+            cfg["flops_executed_per_token"] = "8*V*d (logits recomputed in the shard backward)"
+        if args.path == "norm":
+            cfg["norm"] = "zero-centred RMSNorm of x [N, d] in front of the head (eps 1e-6)"
     if getattr(args, "slices", 0) > 0:
         cfg["dw_slices"] = args.slices
         cfg["sm_limit"] = args.sm_limit
@@ -216,6 +223,12 @@ def main():
                     help="finish dW in this many vocabulary slices (lce_fwd_bwd_sliced); with --gpus > 1 the "
                          "FSDP-style step: dW reduced to its row owners slice by slice on a side stream")
     ap.add_argument("--sm-limit", type=int, default=0, help="with --slices: SMs the GEMM launches may use (0 = all)")
+    ap.add_argument("--path", default="fused", choices=["fused", "norm", "vshard"],
+                    help="fused: lce_fwd_bwd (the metric's step); norm: final RMSNorm + LM head + CE "
+                         "(lce_norm_fwd_bwd, x in place of H); vshard: the vocabulary-parallel calls with "
+                         "--shards shards run in turn on one GPU (partial dH summed by torch in place of the "
+                         "all-reduce)")
+    ap.add_argument("--shards", type=int, default=4, help="with --path vshard: number of vocabulary shards")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -262,7 +275,29 @@ def main():
     slice_events = [torch.cuda.Event() for _ in range(len(bounds) - 1)] if bounds else None
     comm = torch.cuda.Stream(dev) if (bounds and world > 1) else None
 
+    if args.path != "fused" and (world > 1 or bounds):
+        raise SystemExit("--path norm / vshard run on one GPU without --slices")
+    if args.path == "norm":
+        w_norm = torch.from_numpy(np.random.default_rng(w.seed + 1).normal(0.0, 0.1, d).astype(np.float32)).to(dev)
+        ws_norm = torch.empty(lce.workspace_size(lce.LCE_OP_NORM_FWD_BWD, N, d, V, lce.make_opts(**opts)),
+                              dtype=torch.uint8, device=dev)
+    shard_cuts = [V * r // args.shards // 8 * 8 for r in range(args.shards)] + [V]
+
     def step(Hx, yx):
+        if args.path == "norm":
+            loss, _, dx, _, _ = lce.lce_norm_fwd_bwd(Hx, w_norm, W, yx, dW=dW, workspace=ws_norm, **opts)
+            return loss, dx
+        if args.path == "vshard":
+            cuts = shard_cuts
+            stats = [lce.lce_vshard_forward_stats(Hx, W[cuts[r]:cuts[r + 1]], yx, cuts[r], V, chunk_tokens=chunk)
+                     for r in range(args.shards)]
+            loss, lse_v = lce.lce_vshard_combine(torch.stack(stats), yx, V)
+            dH = None
+            for r in range(args.shards):
+                part, _ = lce.lce_vshard_backward(Hx, W[cuts[r]:cuts[r + 1]], yx, cuts[r], V, lse_v,
+                                                  dW=dW[cuts[r]:cuts[r + 1]], chunk_tokens=chunk)
+                dH = part if dH is None else dH.add_(part)
+            return loss, dH
         if bounds and world > 1:
             loss, _, dH, _ = fsdp.fsdp_fwd_bwd(Hx, W, yx, owners=owners, slices=bounds, comm_stream=comm,
                                                sm_limit=args.sm_limit, dW=dW, lse=lse, workspace=ws,
@@ -365,6 +400,14 @@ def main():
                    "share": round(v["ms"] / total_ms, 4) if total_ms else 0.0}
                for k, v in prof.items() if v["launches"]}
     gpu_launches = sum(v["launches"] for k, v in prof.items() if k != "other")
+    hbm_kernels = {}
+    for k in lce.HBM_KINDS:
+        v = prof.get(k)
+        if v and v["launches"] and v["ms"] > 0:
+            gbs = v["work"] / (v["ms"] * 1e-3) / 1e9
+            hbm_kernels[k] = {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": gbs / peaks["hbm_gbs"], "bytes_per_launch": v["work"] / v["launches"],
+                              "ms_per_launch": v["ms"] / v["launches"]}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -374,6 +417,7 @@ def main():
         "pct_of_bf16_peak_sustained": tflops / peaks["bf16_tflops_sustained"],
         "peak_source": peak_src, "flops_per_step": flops_step,
         "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches, "e2e": e2e, "clocks": clk,
+        **({"hbm_kernels": hbm_kernels} if hbm_kernels else {}),
         "extra_device_bytes": int(ws.numel()), "unfused_logits_bytes": N * V * 4,
     }
     if world == 1 and not args.no_cpu_baseline:

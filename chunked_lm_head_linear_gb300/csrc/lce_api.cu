@@ -214,15 +214,16 @@ enum Kind : int {
   K_COMBINE = 2,
   K_LOGITS_GRAD = 3,    // unconditional FWD_GRAD (lce_backward)
   K_GEMM_BWD = 4,       // dH and dW GEMMs of a chunk (one launch)
-  K_RESERVED = 5,
+  K_RMSNORM_FWD = 5,
   K_FINALIZE = 6,
-  K_OTHER = 7,          // memsets, the guard-conditional FWD_GRAD (work counted as 0), RMSNorm kernels
+  K_OTHER = 7,          // memsets, the guard-conditional FWD_GRAD (work counted as 0), gradient scaling
   K_LOGITS_REF = 8,
   K_HSCALE = 9,
+  K_RMSNORM_BWD = 10,   // norm backward and the column sum of its dw partials
 };
-const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",  "logits_stats", "combine",    "logits_grad",
-                                                  "gemm_dH_dW", "reserved",   "finalize",   "other",
-                                                  "logits_ref", "hscale"};
+const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",    "logits_stats", "combine",  "logits_grad",
+                                                  "gemm_dH_dW", "rmsnorm_fwd",  "finalize", "other",
+                                                  "logits_ref", "hscale",       "rmsnorm_bwd"};
 
 struct ProfRecord {
   int kind;
@@ -772,7 +773,7 @@ int lce_rmsnorm_forward(const void* x, const float* w, int64_t N, int64_t d, flo
   DeviceInfo dev;
   LCE_TRY(device_check(&dev));
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return timed(s, K_OTHER, 4.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N), [&] {
+  return timed(s, K_RMSNORM_FWD, 4.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N + d), [&] {
     return cuda_rc(lce::launch_rmsnorm_fwd(x, w, N, static_cast<int>(d), eps, H, rstd, s));
   });
 }
@@ -788,7 +789,7 @@ int lce_rmsnorm_backward(const void* x, const float* w, const float* rstd, const
   DeviceInfo dev;
   LCE_TRY(device_check(&dev));
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return timed(s, K_OTHER, 6.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N + d), [&] {
+  return timed(s, K_RMSNORM_BWD, 6.0 * static_cast<double>(N * d) + 4.0 * static_cast<double>(N + 2 * d), [&] {
     return cuda_rc(lce::launch_rmsnorm_bwd(x, w, rstd, dH, N, static_cast<int>(d), dx, dw, static_cast<float*>(ws),
                                            s));
   });

@@ -40,9 +40,11 @@ EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward"
             "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward",
             "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd",
             "lce_scale_grads", "lce_fwd_bwd_sliced")
-LCE_KERNEL_KINDS = 10
+LCE_KERNEL_KINDS = 11
 # Kernel kinds whose profiled work is flops (tensor-core GEMMs); the others count bytes.
 GEMM_KINDS = ("logits_stats", "logits_grad", "gemm_dH_dW", "logits_ref")
+# HBM-bound kernels whose profiled work is bytes and which bench.py reports on their own.
+HBM_KINDS = ("rmsnorm_fwd", "rmsnorm_bwd")
 
 
 class LceOpts(ctypes.Structure):

@@ -271,7 +271,7 @@ int lce_version(void);
  * Events come from a pool the library owns (created on first use, no device
  * memory is allocated). Not thread-safe: one profiling thread at a time.
  */
-#define LCE_KERNEL_KINDS 10
+#define LCE_KERNEL_KINDS 11
 typedef struct lce_profile {
   int32_t launches[LCE_KERNEL_KINDS];
   double ms[LCE_KERNEL_KINDS];      /* summed device time per kind */
