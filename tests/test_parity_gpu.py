@@ -103,6 +103,7 @@ RAGGED = [
     (1, 64, 300, 0),         # a single token
     (40, 8, 2, 0),           # two classes, d = 8 (smallest legal hidden size)
     (200, 512, 257, 0),      # vocabulary one past a tile
+    (37, 16, 1, 0),          # a single class: loss 0, zero gradients
 ]
 
 
@@ -360,7 +361,9 @@ def _stratified_vocab(V, y, rng, k=128):
     return np.unique(np.concatenate(picks))
 
 
-def sampled_full_check(cuda_lib, name, chunk_tokens=0):
+def sampled_full_check(cuda_lib, name, chunk_tokens=0, compute=None):
+    """``compute(H, W, y) -> (loss, lse, dH, dW)`` on the device; by default the
+    fused call ``lce_fwd_bwd`` with ``chunk_tokens``."""
     torch = _torch()
     gpath = os.path.join(GOLDEN, f"full_{name}.npz")
     if not os.path.exists(gpath):
@@ -372,7 +375,10 @@ def sampled_full_check(cuda_lib, name, chunk_tokens=0):
     w = inp["workload"]
     y_np = inp["y"]
     H, W, y = to_dev(inp)
-    loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=chunk_tokens, sync_check=True)
+    if compute is None:
+        loss, lse, dH, dW = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=chunk_tokens, sync_check=True)
+    else:
+        loss, lse, dH, dW = compute(H, W, y)
     torch.cuda.synchronize()
     # loss and every lse against the oracle
     assert abs(loss.item() - float(gold["loss"])) <= TOL_LOSS * abs(float(gold["loss"]))
@@ -405,6 +411,70 @@ def sampled_full_check(cuda_lib, name, chunk_tokens=0):
 
 def test_full_qwen2b_workload(cuda_lib):
     sampled_full_check(cuda_lib, "qwen2b_n8192_d2048_v151936")
+
+
+def test_full_qwen2b_vocab_shards(cuda_lib):
+    """The vocabulary-parallel calls at the bench workload, four uneven shards
+    run in turn on one GPU (the launch configuration of bench.py --path vshard):
+    per-shard statistics, the rank-order merge, the shard backward; the partial
+    dH summed by torch in place of the all-reduce."""
+    torch = _torch()
+
+    def shards(H, W, y):
+        V = W.shape[0]
+        cuts = [0, 37000, 76032, 114000, V]
+        stats = [cuda_lib.lce_vshard_forward_stats(H, W[a:b], y, a, V, chunk_tokens=4096)
+                 for a, b in zip(cuts[:-1], cuts[1:])]
+        loss, lse = cuda_lib.lce_vshard_combine(torch.stack(stats), y, V)
+        dW = torch.empty((V, W.shape[1]), dtype=torch.float32, device="cuda")
+        dH = None
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            part, _ = cuda_lib.lce_vshard_backward(H, W[a:b], y, a, V, lse, dW=dW[a:b], chunk_tokens=4096)
+            dH = part if dH is None else dH.add_(part)
+        return loss, lse, dH, dW
+
+    sampled_full_check(cuda_lib, "qwen2b_n8192_d2048_v151936", compute=shards)
+
+
+def test_full_qwen2b_norm_fwd_bwd(cuda_lib):
+    """Final RMSNorm + head at the bench workload's size (x = the workload's
+    hidden states, w ~ N(0, 0.1), eps 1e-6): lse and dx on sampled rows against
+    the oracle (norm -> bf16 H -> rows of the cross-entropy -> norm backward),
+    the loss from the GPU's lse and the oracle's label logits, dW on sampled
+    vocabulary rows, and dw_norm through sum_k (1 + w_k) dw_k = <dH, H> = <dW, W>."""
+    torch = _torch()
+    name = "qwen2b_n8192_d2048_v151936"
+    inp = inputs.make_inputs(name)
+    wl = inp["workload"]
+    y_np = inp["y"]
+    wn = np.random.default_rng(99).normal(0.0, 0.1, wl.d).astype(np.float32)
+    x, W, y = to_dev(inp)
+    loss, lse, dx, dw_norm, dW = cuda_lib.lce_norm_fwd_bwd(x, torch.from_numpy(wn).cuda(), W, y, eps=1e-6,
+                                                           chunk_tokens=4096, sync_check=True)
+    torch.cuda.synchronize()
+    xf = inputs.bf16_bits_to_f32(inp["H"]).astype(np.float64)
+    Wf = inputs.bf16_bits_to_f32(inp["W"])
+    h, r = oracle.rmsnorm_f64(xf, wn.astype(np.float64), 1e-6)
+    Hb = oracle.decode_bf16(oracle.round_bf16_bits(h))
+    scale, n = oracle.grad_scale(y_np)
+    rng = np.random.default_rng(321)
+    R = _stratified_rows(y_np, wl.N, rng)
+    fw = oracle.forward_rows_f64(Hb, Wf, y_np, R)
+    lse_gpu = lse.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(lse_gpu[R] - fw["lse"]) / np.maximum(np.abs(fw["lse"]), 1.0)) <= TOL_LSE
+    valid = y_np != oracle.IGNORE_INDEX
+    z_y = np.einsum("ij,ij->i", Hb[valid], Wf.astype(np.float64)[y_np[valid]])
+    loss_from_lse = float((lse_gpu[valid] - z_y).sum() / n)
+    assert abs(loss.item() - loss_from_lse) <= TOL_LOSS * abs(loss_from_lse)
+    dH_R = oracle.dH_rows_f64(Hb, Wf, y_np, R, scale)
+    dx_R, _ = oracle.rmsnorm_backward_f64(xf[R], wn.astype(np.float64), r[R], dH_R)
+    assert rel_fro(dx[torch.from_numpy(R).cuda()].float().cpu().numpy(), dx_R) <= TOL_GRAD
+    S = _stratified_vocab(wl.V, y_np, rng)
+    dW_ref = oracle.dW_rows_f64(Hb, Wf, y_np, lse_gpu, S, scale)
+    assert rel_fro(dW[torch.from_numpy(S).cuda()].cpu().numpy(), dW_ref) <= TOL_GRAD
+    a = float((torch.from_numpy(1.0 + wn.astype(np.float64)).cuda() * dw_norm.double()).sum().item())
+    b = (dW.double() * W.double()).sum().item()
+    assert abs(a - b) <= TOL_GRAD * max(abs(a), abs(b))
 
 
 @pytest.mark.slow
