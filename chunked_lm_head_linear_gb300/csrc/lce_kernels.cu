@@ -693,10 +693,14 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   const long long nH = static_cast<long long>(p.h_m) * p.h_n, nW = p.w_tiles;
   const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
   if (P <= 0) return cudaSuccess;
-  // Balance: every cluster should end with ~(nH h_k + nW w_k) / P k-blocks.
-  const double target = (static_cast<double>(nH) * p.h_k + static_cast<double>(nW) * p.w_k) / P;
+  // Balance: every cluster should end with the same share of the launch's time. A dH k-block (A
+  // K-major, B N-major) runs in ~0.93 of a dW k-block's time (both N-major): 637 vs 685 SM cycles
+  // per 64-deep k-block, measured on the Qwen3.5-2B-like head with cycle counters in the MMA issuer.
+  constexpr double kDhKblockCost = 0.93;
+  const double h_cost = kDhKblockCost * p.h_k, w_cost = p.w_k;
+  const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
   const long long hmax = (nH + P - 1) / P;
-  long long q1 = static_cast<long long>((target - static_cast<double>(hmax) * p.h_k) / p.w_k);
+  long long q1 = static_cast<long long>((target - static_cast<double>(hmax) * h_cost) / w_cost);
   if (q1 < 0) q1 = 0;
   if (q1 > nW / P) q1 = nW / P;
   p.w_phase1 = static_cast<int>(q1 * P);
