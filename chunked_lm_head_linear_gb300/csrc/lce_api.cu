@@ -9,17 +9,18 @@
 // introduction", memory optimisation section):
 //   prepare                      label scan -> n, g/n, range-error bit
 //   for each chunk of C tokens:
-//     logits GEMM (FWD_REF)      row reference: max over the first vocabulary tile
+//     logits GEMM (FWD_REF)      row reference: max over the first 128 words
 //     logits GEMM (FWD_STATS_P)  per-tile (max, sum-exp), z_{i,y_i}, exp tile P
 //     combine                    lse_i, loss_i, alpha_i = exp(ref_i - lse_i), label entry of P
 //     logits GEMM (FWD_GRAD)     only if a logit exceeded its reference by > 60 nats:
 //                                the exact gradient tile replaces P (alpha = 1)
 //     hscale                     Ht = alpha * H_c
-//     dH GEMM                    dH_c = (g/n) alpha (P W)
-//     dW GEMM                    dW (+)= (g/n) P^T Ht
+//     backward GEMMs (one launch) dH_c = (g/n) alpha (P W) and dW (+)= (g/n) P^T Ht
 //   finalize                     loss = sum_i loss_i / n
 // lce_forward runs prepare, FWD_STATS + combine per chunk, finalize;
-// lce_backward recomputes: FWD_GRAD (from the saved lse), dH and dW GEMMs.
+// lce_backward recomputes: FWD_GRAD (from the saved lse), then the backward
+// GEMMs. lce_fwd_bwd_sliced issues the last chunk's backward GEMMs as one
+// launch per vocabulary slice of dW and records an event after each.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -8,7 +8,7 @@
 // ("XTuner on Ascend 910C: Qwen3.5-2B training optimisation", section 3.1.4:
 // the logits chunk, and the backward's d_input / d_weight.)
 //
-// The kernel runs on clusters of two CTAs (one TPC each) and computes 256 x 256
+// The kernel runs on clusters of two CTAs (the two SMs of one TPC) and computes 256 x 256
 // output tiles with tcgen05.mma.cta_group::2. Each CTA has 384 threads:
 //   warp 0      TMA producer (one thread): its CTA's half of the A/B k-blocks
 //   warp 1      MMA issuer (one thread, even CTA of the pair)

@@ -29,7 +29,7 @@ enum FwdMode : int {
   FWD_STATS = 0,    // per-(row, vocab tile) max / sum-exp partials + target logit
   FWD_STATS_P = 1,  // FWD_STATS + exp-tile P = bf16(exp(z - ref_row)) stored for the backward
   FWD_GRAD = 2,     // gradient tile exp(z - lse) - onehot (valid rows), from a known lse
-  FWD_REF = 3,      // row maximum over the first vocabulary tile
+  FWD_REF = 3,      // row maximum over the first 128 words (one launch over the first tile)
 };
 
 // An exp-tile entry may exceed the row reference by at most this many nats;

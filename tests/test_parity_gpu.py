@@ -127,7 +127,7 @@ def test_large_logits_and_zipf_labels(cuda_lib):
 
 def test_reference_guard_falls_back_to_exact_gradient(cuda_lib):
     """The fused call stores exp(z - ref) with ref = the row's maximum over the
-    first 256 words. A word outside that tile whose logits reach ~80 sigma
+    first 128 words. A word outside them whose logits reach ~80 sigma
     above it trips the guard; the chunk must then use the exact gradient tile
     and still match the oracle."""
     inp = small_inputs(300, 64, 1000, seed=17, sigma_w=0.05)
