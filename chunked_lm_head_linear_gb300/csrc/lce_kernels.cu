@@ -700,9 +700,22 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   const double h_cost = kDhKblockCost * p.h_k, w_cost = p.w_k;
   const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
   const long long hmax = (nH + P - 1) / P;
-  long long q1 = static_cast<long long>((target - static_cast<double>(hmax) * h_cost) / w_cost);
-  if (q1 < 0) q1 = 0;
-  if (q1 > nW / P) q1 = nW / P;
+  const long long r = nH % P, nlight = r == 0 ? P : P - r;
+  // Longest cluster for q dW tiles each in the first phase: the clusters holding hmax dH tiles, or
+  // those holding one fewer that take the second phase's tiles round-robin.
+  auto longest = [&](long long q) {
+    const long long rem = nW - q * P;
+    const long long c2 = rem > 0 ? (rem + nlight - 1) / nlight : 0;
+    const double light = static_cast<double>(r == 0 ? hmax : hmax - 1) * h_cost + static_cast<double>(q + c2) * w_cost;
+    const double heavy = static_cast<double>(hmax) * h_cost + static_cast<double>(q) * w_cost;
+    return r == 0 ? light : (heavy > light ? heavy : light);
+  };
+  long long q0 = static_cast<long long>((target - static_cast<double>(hmax) * h_cost) / w_cost);
+  if (q0 < 0) q0 = 0;
+  if (q0 > nW / P) q0 = nW / P;
+  long long q1 = q0;
+  for (long long q = q0 > 0 ? q0 - 1 : 0; q <= q0 + 1 && q <= nW / P; ++q)
+    if (longest(q) < longest(q1)) q1 = q;
   p.w_phase1 = static_cast<int>(q1 * P);
   return launch_pair<BwdProb>(p, P, s);
 }
