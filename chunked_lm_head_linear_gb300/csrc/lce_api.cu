@@ -8,13 +8,13 @@
 // optimisation", section 3.1.4; tokens in chunks as in "XTuner V1
 // introduction", memory optimisation section):
 //   prepare                      label scan -> n, g/n, range-error bit
+//   logits GEMM (FWD_REF)        row reference of every row: max over the first 128 words
 //   for each chunk of C tokens:
-//     logits GEMM (FWD_REF)      row reference: max over the first 128 words
 //     logits GEMM (FWD_STATS_P)  per-tile (max, sum-exp), z_{i,y_i}, exp tile P
-//     combine                    lse_i, loss_i, alpha_i = exp(ref_i - lse_i), label entry of P
+//     combine                    lse_i, loss_i, alpha_i = exp(ref_i - lse_i), label entry of P,
+//                                Ht = alpha * H_c
 //     logits GEMM (FWD_GRAD)     only if a logit exceeded its reference by > 60 nats:
 //                                the exact gradient tile replaces P (alpha = 1)
-//     hscale                     Ht = alpha * H_c
 //     backward GEMMs (one launch) dH_c = (g/n) alpha (P W) and dW (+)= (g/n) P^T Ht
 //   finalize                     loss = sum_i loss_i / n
 // lce_forward runs prepare, FWD_STATS + combine per chunk, finalize;
@@ -104,7 +104,7 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
   L.chunks = N > 0 ? ceil_div(N, L.C) : 0;
   if (op == LCE_OP_FWD_BWD) {
     L.lse = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
-    L.ref = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.ref = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
     L.alpha = take(sizeof(float) * static_cast<size_t>(L.C));
     L.guard = take(sizeof(int) * static_cast<size_t>(L.chunks > 0 ? L.chunks : 1));
     L.Ht = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(d));
@@ -219,12 +219,12 @@ enum Kind : int {
   K_FINALIZE = 6,
   K_OTHER = 7,          // memsets, the guard-conditional FWD_GRAD (work counted as 0), gradient scaling
   K_LOGITS_REF = 8,
-  K_HSCALE = 9,
+  K_UNUSED = 9,         // (formerly the separate Ht = alpha H pass, now inside combine)
   K_RMSNORM_BWD = 10,   // norm backward and the column sum of its dw partials
 };
 const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",    "logits_stats", "combine",  "logits_grad",
                                                   "gemm_dH_dW", "rmsnorm_fwd",  "finalize", "other",
-                                                  "logits_ref", "hscale",       "rmsnorm_bwd"};
+                                                  "logits_ref", "unused",       "rmsnorm_bwd"};
 
 struct ProfRecord {
   int kind;
@@ -438,28 +438,27 @@ int backward_chunk(const Call& c, int64_t c0, int64_t rows, const float* lse, vo
 int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* lse, float* loss_i, uint16_t* dH,
                 float* dW, bool accumulate, const Slices* sl = nullptr) {
   uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
-  float* ref = reinterpret_cast<float*>(c.ws + c.L.ref);
+  float* ref = reinterpret_cast<float*>(c.ws + c.L.ref) + c0;  // row references of every row, computed up front
   float* alpha = reinterpret_cast<float*>(c.ws + c.L.alpha);
   int* guard = reinterpret_cast<int*>(c.ws + c.L.guard) + chunk;
   uint16_t* Ht = reinterpret_cast<uint16_t*>(c.ws + c.L.Ht);
 
   LogitsArgs a;
-  a.mode = lce::FWD_REF;
-  a.ref = ref;
-  LCE_TRY(logits_gemm(c, c0, rows, a));
-
   a.mode = lce::FWD_STATS_P;
+  a.ref = ref;
   a.P = P;
   a.guard = guard;
   LCE_TRY(logits_gemm(c, c0, rows, a));
 
-  const double cbytes = static_cast<double>(rows) * (16.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2);
+  const double cbytes = static_cast<double>(rows) *
+                        (16.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2 + 4.0 * static_cast<double>(c.d));
   LCE_TRY(timed(c.s, K_COMBINE, cbytes, [&] {
-    return cuda_rc(lce::launch_combine_exp(reinterpret_cast<const float2*>(c.ws + c.L.partials),
-                                           static_cast<int>(2 * c.L.T), static_cast<int>(rows),
-                                           reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0,
-                                           static_cast<int>(c.V), c.o.ignore_index, ref, guard, lse + c0, loss_i + c0,
-                                           alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp, c.s));
+    return cuda_rc(lce::launch_combine_exp(
+        reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(2 * c.L.T), static_cast<int>(rows),
+        reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0, static_cast<int>(c.V), c.o.ignore_index, ref,
+        guard, lse + c0, loss_i + c0, alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp,
+        reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), static_cast<int>(c.d),
+        reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
   }));
 
   LogitsArgs g;
@@ -469,14 +468,17 @@ int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* l
   g.only_if = guard;
   LCE_TRY(logits_gemm(c, c0, rows, g));
 
-  const double hbytes = static_cast<double>(rows) * static_cast<double>(c.d) * 4.0 + 4.0 * static_cast<double>(rows);
-  LCE_TRY(timed(c.s, K_HSCALE, hbytes, [&] {
-    return cuda_rc(lce::launch_hscale(reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), alpha,
-                                      static_cast<int>(rows), static_cast<int>(c.d),
-                                      reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
-  }));
   if (sl) return dh_dw_sliced(c, c0, rows, alpha, Ht, dH, dW, accumulate, *sl);
   return dh_dw(c, c0, rows, alpha, Ht, dH, dW, accumulate);
+}
+
+// Row references m~_i for all N rows in one launch (one round of 256-row tiles
+// over the first vocabulary tile), before the chunk loop.
+int row_references(const Call& c) {
+  LogitsArgs a;
+  a.mode = lce::FWD_REF;
+  a.ref = reinterpret_cast<float*>(c.ws + c.L.ref);
+  return logits_gemm(c, 0, c.N, a);
 }
 
 int prepare(const Call& c, const float* grad_loss) {
@@ -625,6 +627,7 @@ int fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d
     LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
                   [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
   if (N == 0) LCE_TRY(record_slice_events(c, sl, 0));
+  if (N > 0) LCE_TRY(row_references(c));
   for (int64_t k = 0, c0 = 0; c0 < N; ++k, c0 += c.L.C) {
     const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
     const bool last = c0 + rows >= N;

@@ -309,6 +309,7 @@ __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ part
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
     merge_ms(m, s, m2, s2);
   }
+  float a = 0.f;  // alpha_i, decided by lane 0
   if (lane == 0) {
     const float l = m + logf(s);
     lse[r] = l;
@@ -328,7 +329,9 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
                                                      int V, long long ignore_index, const float* __restrict__ ref,
                                                      const int* __restrict__ guard, float* __restrict__ lse,
                                                      float* __restrict__ loss_i, float* __restrict__ alpha,
-                                                     __nv_bfloat16* __restrict__ P, long long ldp) {
+                                                     __nv_bfloat16* __restrict__ P, long long ldp,
+                                                     const uint4* __restrict__ H, int groups_per_row,
+                                                     uint4* __restrict__ Ht) {
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -343,13 +346,13 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
     merge_ms(m, s, m2, s2);
   }
+  float a = 0.f;  // alpha_i, decided by lane 0
   if (lane == 0) {
     const float l = m + logf(s);
     lse[r] = l;
     const long long yr = y[r];
     const bool valid = yr != ignore_index && yr >= 0 && yr < V;
     loss_i[r] = valid ? l - ztgt[r] : 0.f;
-    float a = 0.f;
     if (valid) {
       if (*guard != 0) {
         a = 1.f;
@@ -362,27 +365,23 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
     }
     alpha[r] = a;
   }
+  // Ht_i = bf16(alpha_i H_i): the B operand of the dW GEMM (the whole warp, 16 bytes per lane)
+  a = __shfl_sync(0xffffffffu, a, 0);
+  const uint4* hr = H + static_cast<long long>(r) * groups_per_row;
+  uint4* tr = Ht + static_cast<long long>(r) * groups_per_row;
+  for (int g = lane; g < groups_per_row; g += 32) {
+    const uint4 h = hr[g];
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * a, __uint_as_float(w[q] & 0xffff0000u) * a);
+    tr[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // Ht_r = bf16(alpha_r * H_r): the per-row softmax scale moved onto the dW
 // GEMM's B operand (dW = P^T Ht). Eight bf16 per thread; d % 8 == 0.
-__global__ void __launch_bounds__(256) k_hscale(const uint4* __restrict__ H, const float* __restrict__ alpha,
-                                                long long groups, int groups_per_row, uint4* __restrict__ Ht) {
-  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < groups;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const float a = alpha[i / groups_per_row];
-    const uint4 h = H[i];
-    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float lo = __uint_as_float(w[q] << 16) * a;
-      const float hi = __uint_as_float(w[q] & 0xffff0000u) * a;
-      o[q] = pack_bf16x2(lo, hi);
-    }
-    Ht[i] = make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
 
 // One warp per row: this vocabulary shard's (max, sum-exp) over its columns,
 // its logit of the label if the label lies in the shard, and whether it does.
@@ -738,25 +737,17 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
 
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
-                               float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp, cudaStream_t s) {
+                               float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp,
+                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
   k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, ref, guard,
-                                                       lse, loss_i, alpha, P, ldp);
+                                                       lse, loss_i, alpha, P, ldp, reinterpret_cast<const uint4*>(H),
+                                                       d / 8, reinterpret_cast<uint4*>(Ht));
   return cudaGetLastError();
 }
 
-cudaError_t launch_hscale(const __nv_bfloat16* H, const float* alpha, int rows, int d, __nv_bfloat16* Ht,
-                          cudaStream_t s) {
-  const long long groups = static_cast<long long>(rows) * (d / 8);
-  if (groups <= 0) return cudaSuccess;
-  long long blocks = (groups + 255) / 256;
-  if (blocks > 152 * 8) blocks = 152 * 8;
-  k_hscale<<<static_cast<int>(blocks), 256, 0, s>>>(reinterpret_cast<const uint4*>(H), alpha, groups, d / 8,
-                                                    reinterpret_cast<uint4*>(Ht));
-  return cudaGetLastError();
-}
 
 cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                long long y_offset, int V_shard, int V_total, long long ignore_index, float4* stats,
