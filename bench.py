@@ -178,7 +178,7 @@ def run_reference(args, w):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": config_of(w, None, args),
+            "data": "synthetic", "config": config_of(w, min(args.chunk, w.N) if args.chunk > 0 else 0, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{rows} tokens per step at full d and V (numpy fp64 oracle, fwd+bwd)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
