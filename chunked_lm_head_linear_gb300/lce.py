@@ -191,7 +191,39 @@ def _check_inputs(H, W, y):
         raise ValueError("shapes must be H [N, d], W [V, d], y [N]")
     if not (H.is_contiguous() and W.is_contiguous() and y.is_contiguous()):
         raise ValueError("H, W and y must be contiguous")
+    if not (H.device == W.device == y.device):
+        raise ValueError("H, W and y must be on the same device")
+    if H.device.index != torch.cuda.current_device():
+        raise ValueError(f"the inputs are on {H.device}; make it the current device (torch.cuda.set_device)")
     return H.shape[0], H.shape[1], W.shape[0]
+
+
+def _check_grads(H, N, d, V, *, lse=None, grad_loss=None, dW=None, lse_needs_n=True):
+    import torch
+    _check_dev(lse, "lse", torch.float32, numel=N if lse_needs_n else None, device=H.device)
+    _check_dev(grad_loss, "grad_loss", torch.float32, numel=1, device=H.device)
+    _check_dev(dW, "dW", torch.float32, shape=(V, d), device=H.device)
+
+
+def _check_dev(t, name, dtype, numel=None, shape=None, device=None):
+    """A caller-supplied tensor the kernels read or write: CUDA, the given dtype,
+    contiguous, on ``device``, and with the shape (or at least ``numel``
+    elements) the call needs, so that no kernel touches memory past it."""
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, the inputs on {device}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if numel is not None and t.numel() < numel:
+        raise ValueError(f"{name} needs at least {numel} elements, has {t.numel()}")
 
 
 def _workspace(op, N, d, V, opts, device, workspace=None):
@@ -199,6 +231,8 @@ def _workspace(op, N, d, V, opts, device, workspace=None):
     need = workspace_size(op, N, d, V, opts)
     if need == 0:
         raise LCEError(LCE_ERR_INVALID_ARG, "lce_workspace_size")
+    if workspace is not None:
+        _check_dev(workspace, "workspace", torch.uint8, device=device)
     if workspace is not None and workspace.numel() >= need:
         return workspace
     # torch's allocator returns 512-byte aligned blocks
@@ -231,6 +265,9 @@ def lce_backward(H, W, y, lse, grad_loss=None, *, dW=None, workspace=None, strea
     device fp32 scalar tensor or None (1.0)."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    _check_grads(H, N, d, V, lse=lse, grad_loss=grad_loss, dW=dW)
+    if N > 0 and lse is None:
+        raise ValueError("lse is required")
     if "chunk_tokens" in opt_kw:
         opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
@@ -248,6 +285,7 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
     """loss, lse, dH, dW in one call."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    _check_grads(H, N, d, V, lse=lse, grad_loss=grad_loss, dW=dW)
     if "chunk_tokens" in opt_kw:
         opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
@@ -287,6 +325,7 @@ def lce_fwd_bwd_sliced(H, W, y, grad_loss=None, *, bounds, events=None, sm_limit
     [bounds[s], bounds[s+1]) are final. Same outputs as lce_fwd_bwd, bit for bit."""
     import torch
     N, d, V = _check_inputs(H, W, y)
+    _check_grads(H, N, d, V, lse=lse, grad_loss=grad_loss, dW=dW)
     if "chunk_tokens" in opt_kw:
         opt_kw["chunk_tokens"] = _resolve_chunk(opt_kw["chunk_tokens"], N, d, V, H.device)
     opts = make_opts(**opt_kw)
@@ -360,11 +399,15 @@ def lce_vshard_forward_stats(H, W_shard, y, vocab_offset: int, V_total: int, *, 
 def lce_vshard_combine(stats_all, y, V_total: int, *, workspace=None, stream=None, **opt_kw):
     """Merge the shards' statistics [R, N, 4] (rank order) into lse [N] and the loss [1]."""
     import torch
+    if not (isinstance(stats_all, torch.Tensor) and stats_all.dim() == 3 and stats_all.shape[2] == 4):
+        raise ValueError("stats_all must be an fp32 CUDA tensor [R, N, 4]")
     R, N = int(stats_all.shape[0]), int(stats_all.shape[1])
-    if not (stats_all.is_cuda and stats_all.dtype == torch.float32 and stats_all.is_contiguous()):
-        raise ValueError("stats_all must be a contiguous fp32 CUDA tensor [R, N, 4]")
+    _check_dev(stats_all, "stats_all", torch.float32)
+    _check_dev(y, "y", torch.int64, shape=(N,), device=stats_all.device)
     opts = make_opts(**opt_kw)
     need = workspace_size(LCE_OP_VSHARD_COMBINE, N, 8, V_total, opts)
+    if workspace is not None:
+        _check_dev(workspace, "workspace", torch.uint8, device=stats_all.device)
     ws = workspace if workspace is not None and workspace.numel() >= need else \
         torch.empty(need, dtype=torch.uint8, device=stats_all.device)
     lse = torch.empty(max(N, 1), dtype=torch.float32, device=stats_all.device)[:N]
@@ -380,6 +423,9 @@ def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, gra
     """This shard's dW [V_shard, d] and its fp32 partial dH [N, d] (sum over shards = dH)."""
     import torch
     N, d, Vs = _check_inputs(H, W_shard, y)
+    _check_grads(H, N, d, Vs, lse=lse, grad_loss=grad_loss, dW=dW)
+    if N > 0 and lse is None:
+        raise ValueError("lse is required")
     opts = make_opts(**opt_kw)
     ws = _workspace(LCE_OP_BACKWARD, N, d, Vs, opts, H.device, workspace)
     dH = torch.empty((N, d), dtype=torch.float32, device=H.device)
@@ -401,6 +447,8 @@ def _check_norm(x, w):
         raise ValueError("x must be a bf16 CUDA tensor [N, d], w an fp32 CUDA tensor [d]")
     if x.dim() != 2 or w.dim() != 1 or w.shape[0] != x.shape[1] or not (x.is_contiguous() and w.is_contiguous()):
         raise ValueError("shapes must be x [N, d], w [d], contiguous")
+    if x.device != w.device or x.device.index != torch.cuda.current_device():
+        raise ValueError("x and w must be on the current CUDA device")
     return x.shape[0], x.shape[1]
 
 
@@ -419,6 +467,8 @@ def lce_rmsnorm_backward(x, w, rstd, dH, *, stream=None):
     """dx (bf16 [N, d]) and dw (fp32 [d]) of the zero-centred RMSNorm."""
     import torch
     N, d = _check_norm(x, w)
+    _check_dev(rstd, "rstd", torch.float32, numel=N, device=x.device)
+    _check_dev(dH, "dH", torch.bfloat16, shape=(N, d), device=x.device)
     dx = torch.empty_like(x)
     dw = torch.empty(d, dtype=torch.float32, device=x.device)
     need = int(load().lce_rmsnorm_workspace_size(N, d))
@@ -438,6 +488,9 @@ def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, work
     if W.dim() != 2 or W.shape[1] != d or W.dtype != torch.bfloat16 or not W.is_contiguous():
         raise ValueError("W must be a contiguous bf16 [V, d] tensor")
     V = W.shape[0]
+    _check_dev(W, "W", torch.bfloat16, device=x.device)
+    _check_dev(y, "y", torch.int64, shape=(N,), device=x.device)
+    _check_grads(x, N, d, V, grad_loss=grad_loss, dW=dW)
     opts = make_opts(**opt_kw)
     ws = _workspace(LCE_OP_NORM_FWD_BWD, N, d, V, opts, x.device, workspace)
     loss = torch.empty(1, dtype=torch.float32, device=x.device)
@@ -455,6 +508,15 @@ def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, work
 
 def lce_scale_grads(dH, dW, grad_loss, *, stream=None):
     """In place: dH *= g, dW *= g with g = grad_loss[0] read on the device (no-op when g == 1)."""
+    import torch
+    if dH is None and dW is None:
+        return
+    _check_dev(dH, "dH", torch.bfloat16)
+    _check_dev(dW, "dW", torch.float32)
+    _check_dev(grad_loss, "grad_loss", torch.float32, numel=1)
+    if (dH is not None and dH.dim() != 2) or (dW is not None and dW.dim() != 2) or \
+            (dH is not None and dW is not None and dH.shape[1] != dW.shape[1]):
+        raise ValueError("dH must be [N, d] and dW [V, d]")
     N, d = (dH.shape if dH is not None else (0, dW.shape[1]))
     V = dW.shape[0] if dW is not None else 0
     _raise(load().lce_scale_grads(_ptr(dH), _ptr(dW), N, d, V, _ptr(grad_loss), _stream(stream)), "lce_scale_grads")

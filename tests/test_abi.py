@@ -201,3 +201,11 @@ def test_slice_bounds_helper():
     assert lce.slice_bounds(300, 5) == [0, 256, 300]            # no more slices than dW tiles
     with pytest.raises(ValueError):
         lce.slice_bounds(1000, 0)
+
+
+def test_binding_validates_caller_tensors():
+    """A caller's tensor that is not on the GPU is refused before any launch
+    (the dtype / shape / contiguity checks run in the GPU tests)."""
+    torch = pytest.importorskip("torch")
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        lce._check_dev(torch.zeros(4, 8), "dW", torch.float32)

@@ -279,6 +279,27 @@ def test_autograd_wrapper(cuda_lib, recompute):
         assert rel_fro(W.grad.float().cpu().numpy(), ref["dW"]) <= TOL_GRAD
 
 
+def test_binding_rejects_bad_caller_tensors(cuda_lib):
+    """Outputs, saved lse, upstream gradient and workspace passed by the caller
+    are checked before any launch, so a wrong one cannot send a kernel past it."""
+    torch = _torch()
+    inp = small_inputs(64, 64, 300, seed=9)
+    H, W, y = to_dev(inp)
+    bad = [dict(dW=torch.zeros(300, 64, dtype=torch.float64, device="cuda")),
+           dict(dW=torch.zeros(299, 64, device="cuda")),
+           dict(dW=torch.zeros(64, 300, device="cuda").t()),
+           dict(lse=torch.zeros(63, device="cuda")),
+           dict(grad_loss=torch.ones(1, dtype=torch.float64, device="cuda")),
+           dict(workspace=torch.zeros(1 << 20, dtype=torch.float32, device="cuda"))]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            cuda_lib.lce_fwd_bwd(H, W, y, **kw)
+    with pytest.raises(ValueError):
+        cuda_lib.lce_backward(H, W, y, torch.zeros(64, dtype=torch.float16, device="cuda"))
+    with pytest.raises(ValueError):
+        cuda_lib.lce_scale_grads(None, torch.zeros(300, 64, device="cuda"), torch.ones(1, device="cuda").half())
+
+
 def test_all_ignored_and_empty(cuda_lib):
     torch = _torch()
     inp = small_inputs(130, 64, 600, seed=3)
