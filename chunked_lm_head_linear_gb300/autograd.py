@@ -2,7 +2,7 @@
 
     loss_fn = FusedLinearCrossEntropy(ignore_index=-100)
     loss = loss_fn(H, W, y)      # H [N, d] bf16, W [V, d] bf16, y [N] int64, all on the GPU
-    loss.backward()              # H.grad (bf16), W.grad (fp32, accumulated)
+    loss.backward()              # H.grad, W.grad (in W's dtype: autograd casts the fp32 dW to it)
 
 The forward pass runs the whole fused forward + backward (lce_fwd_bwd with an
 upstream gradient of 1) and keeps dH and dW; the backward pass scales them by
@@ -13,6 +13,12 @@ d_input and d_weight, no d_logits is kept), and it costs 6 N V d flops.
 ``recompute=True`` instead saves only lse in the forward and recomputes the
 logits in the backward (lce_backward, 8 N V d flops) -- for when the
 gradients should not be held between the passes.
+
+The library's dW is fp32; autograd hands a leaf its gradient in the leaf's own
+dtype, so a bf16 W receives bf16 gradients. Callers that keep fp32 weight
+gradients (gradient accumulation over micro-batches, fp32 reduction across
+ranks) call ``lce.lce_fwd_bwd`` with their fp32 buffer as ``dW`` and
+``accumulate_dW=True`` instead.
 """
 from __future__ import annotations
 
