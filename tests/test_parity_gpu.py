@@ -186,6 +186,33 @@ def test_gradient_accumulation_over_micro_batches(cuda_lib):
     assert rel_fro(dW.cpu().numpy(), ref["dW"]) <= TOL_GRAD
 
 
+def test_data_parallel_simulated_on_one_gpu(cuda_lib):
+    """Data parallelism over tokens on one GPU: three uneven shards run in turn
+    with the global count of valid labels, their dW and losses summed on the
+    device in rank order. lse and dH are row-local, so they equal the unsharded
+    call bit for bit; loss and dW differ only by fp32 reassociation of the
+    sums (bound TOL_DW_CHUNKING, derived below)."""
+    torch = _torch()
+    inp = small_inputs(700, 256, 4096, seed=41)
+    H, W, y = to_dev(inp)
+    whole = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=128, sync_check=True)
+    n = int((inp["y"] != oracle.IGNORE_INDEX).sum())
+    cuts = [0, 190, 431, 700]
+    loss = torch.zeros(1, device="cuda")
+    dW = torch.zeros_like(whole[3])
+    lses, dHs = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        l_r, lse_r, dH_r, dW_r = cuda_lib.lce_fwd_bwd(H[a:b], W, y[a:b], n_valid_override=n, chunk_tokens=128,
+                                                      sync_check=True)
+        loss += l_r
+        dW += dW_r
+        lses.append(lse_r)
+        dHs.append(dH_r)
+    assert torch.equal(torch.cat(lses), whole[1]) and torch.equal(torch.cat(dHs), whole[2])
+    assert abs(loss.item() - whole[0].item()) <= TOL_DW_CHUNKING * abs(whole[0].item())
+    assert ((dW - whole[3]).norm() / whole[3].norm()).item() <= TOL_DW_CHUNKING
+
+
 def test_auto_chunk(cuda_lib):
     inp = small_inputs(700, 256, 4096, seed=33)
     ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
