@@ -511,7 +511,7 @@ int begin(Call* c, int op, const void* H, const void* W, const int64_t* y, int64
   if (opts) c->o = *opts;
   LCE_TRY(check_sizes(N, d, V, &c->o));
   if (!W || !ws || (N > 0 && (!H || !y))) return LCE_ERR_INVALID_ARG;
-  if (!aligned(W, 16) || (H && !aligned(H, 16)) || (y && !aligned(y, 16)) || !aligned(ws, 256))
+  if (!aligned(W, 16) || (H && !aligned(H, 16)) || (y && !aligned(y, 8)) || !aligned(ws, 256))
     return LCE_ERR_ALIGNMENT;
   c->L = make_layout(op, N, d, V, &c->o);
   if (ws_bytes < c->L.total) return LCE_ERR_WORKSPACE;
@@ -570,7 +570,7 @@ int lce_forward(const void* H, const void* W, const int64_t* y, int64_t N, int64
   Call c;
   LCE_TRY(begin(&c, LCE_OP_FORWARD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
   if (!loss || (N > 0 && !lse)) return LCE_ERR_INVALID_ARG;
-  if (!aligned(loss, 4) || (lse && !aligned(lse, 16))) return LCE_ERR_ALIGNMENT;
+  if (!aligned(loss, 4) || (lse && !aligned(lse, 4))) return LCE_ERR_ALIGNMENT;
   LCE_TRY(device_check(&c.dev));
   LCE_TRY(prepare(c, nullptr));
   float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
@@ -589,7 +589,7 @@ int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int6
   LCE_TRY(begin(&c, LCE_OP_BACKWARD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
   if (c.o.reserved != 0) return LCE_ERR_INVALID_ARG;
   if (!dW || (N > 0 && (!lse || !dH))) return LCE_ERR_INVALID_ARG;
-  if (!aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
+  if (!aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 4)) ||
       (grad_loss && !aligned(grad_loss, 4)))
     return LCE_ERR_ALIGNMENT;
   LCE_TRY(device_check(&c.dev));
@@ -615,7 +615,7 @@ int fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d
   LCE_TRY(begin(&c, LCE_OP_FWD_BWD, H, W, y, N, d, V, opts, ws, ws_bytes, stream));
   if (c.o.reserved != 0) return LCE_ERR_INVALID_ARG;
   if (!loss || !dW || (N > 0 && !dH)) return LCE_ERR_INVALID_ARG;
-  if (!aligned(loss, 4) || !aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 16)) ||
+  if (!aligned(loss, 4) || !aligned(dW, 16) || (dH && !aligned(dH, 16)) || (lse && !aligned(lse, 4)) ||
       (grad_loss && !aligned(grad_loss, 4)))
     return LCE_ERR_ALIGNMENT;
   LCE_TRY(device_check(&c.dev));
@@ -710,8 +710,8 @@ int lce_vshard_combine(const float* stats, int64_t R, const int64_t* y, int64_t 
   LCE_TRY(check_sizes(N, 8, V_total, &c.o));
   if (R <= 0 || R > 4096 || !ws || !loss || (N > 0 && (!stats || !y || !lse)) || c.o.reserved != 0)
     return LCE_ERR_INVALID_ARG;
-  if (!aligned(ws, 256) || (stats && !aligned(stats, 16)) || (lse && !aligned(lse, 16)) || !aligned(loss, 4) ||
-      (y && !aligned(y, 16)))
+  if (!aligned(ws, 256) || (stats && !aligned(stats, 16)) || (lse && !aligned(lse, 4)) || !aligned(loss, 4) ||
+      (y && !aligned(y, 8)))
     return LCE_ERR_ALIGNMENT;
   c.L = make_layout(LCE_OP_VSHARD_COMBINE, N, 8, V_total, &c.o);
   if (ws_bytes < c.L.total) return LCE_ERR_WORKSPACE;
@@ -744,7 +744,7 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
   LCE_TRY(begin(&c, LCE_OP_BACKWARD, H, W_shard, y, N, d, V_shard, opts, ws, ws_bytes, stream));
   LCE_TRY(shard_args(V_shard, vocab_offset, V_total));
   if (c.o.reserved != 0 || !dW_shard || (N > 0 && (!lse || !dH_partial))) return LCE_ERR_INVALID_ARG;
-  if (!aligned(dW_shard, 16) || (dH_partial && !aligned(dH_partial, 16)) || (lse && !aligned(lse, 16)) ||
+  if (!aligned(dW_shard, 16) || (dH_partial && !aligned(dH_partial, 16)) || (lse && !aligned(lse, 4)) ||
       (grad_loss && !aligned(grad_loss, 4)))
     return LCE_ERR_ALIGNMENT;
   c.V_total = V_total;

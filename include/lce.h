@@ -22,8 +22,12 @@
  *   - Pointers named "device" are CUDA device pointers owned by the caller;
  *     the library never allocates, frees or keeps them.
  *   - H [N, d] and W [V, d] are bf16, row-major and contiguous; dH [N, d] is
- *     bf16; dW [V, d], loss [1], lse [N] are fp32; y [N] is int64. All device
- *     pointers must be 16-byte aligned and d a multiple of 8.
+ *     bf16; dW [V, d], loss [1], lse [N] are fp32; y [N] is int64. d is a
+ *     multiple of 8. Alignment: H, W, dH, dW (and x, dx of the norm calls,
+ *     the shard statistics) 16 bytes, because the kernels move them with TMA
+ *     or 16-byte vector accesses; y 8 bytes; lse, loss, grad_loss 4 bytes. A
+ *     slice of rows [a, b) of contiguous H and y therefore always qualifies,
+ *     since a row of H is d * 2 bytes.
  *   - ws / ws_bytes: caller-allocated device workspace of at least
  *     lce_workspace_size(op, ...) bytes, 256-byte aligned. Its contents on
  *     entry do not matter; two calls running at the same time need two
@@ -54,7 +58,7 @@ extern "C" {
 /* status codes */
 #define LCE_OK 0
 #define LCE_ERR_INVALID_ARG 1        /* null pointer, N < 0, d/V <= 0, d % 8 != 0, bad option */
-#define LCE_ERR_ALIGNMENT 2          /* a pointer is not 16-byte (workspace: 256-byte) aligned */
+#define LCE_ERR_ALIGNMENT 2          /* a pointer below the alignment stated below (workspace: 256 bytes) */
 #define LCE_ERR_WORKSPACE 3          /* ws_bytes smaller than lce_workspace_size() */
 #define LCE_ERR_UNSUPPORTED_DEVICE 4 /* the current device is not an sm_103 GPU */
 #define LCE_ERR_CUDA 5               /* a CUDA runtime / driver call failed */

@@ -89,6 +89,8 @@ def test_host_side_argument_errors(lib):
     assert _call_fwd(lib, V=0) == E.LCE_ERR_INVALID_ARG
     assert _call_fwd(lib, N=-5) == E.LCE_ERR_INVALID_ARG
     assert _call_fwd(lib, H=FAKE + 8) == E.LCE_ERR_ALIGNMENT
+    assert _call_fwd(lib, y=FAKE + 4) == E.LCE_ERR_ALIGNMENT           # int64 labels: 8-byte alignment
+    assert _call_fwd(lib, lse=FAKE + 2) == E.LCE_ERR_ALIGNMENT
     assert _call_fwd(lib, ws=FAKE + 64) == E.LCE_ERR_ALIGNMENT
     assert _call_fwd(lib, ws_bytes=16) == E.LCE_ERR_WORKSPACE
     bad = lce.make_opts()
@@ -113,6 +115,8 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
         pytest.skip("a GPU is present")
     rc = _call_fwd(lib)
     assert rc in (lce.LCE_ERR_CUDA, lce.LCE_ERR_UNSUPPORTED_DEVICE)
+    # labels at an odd row offset (8-byte aligned) and lse at any 4-byte boundary are accepted
+    assert _call_fwd(lib, y=FAKE + 8, lse=FAKE + 4) in (lce.LCE_ERR_CUDA, lce.LCE_ERR_UNSUPPORTED_DEVICE)
 
 
 def test_binding_refuses_cpu_tensors():
