@@ -10,11 +10,14 @@
 //   prepare                      label scan -> n, g/n, range-error bit
 //   logits GEMM (FWD_REF)        row reference of every row: max over the first 128 words
 //   for each chunk of C tokens:
-//     logits GEMM (FWD_STATS_P)  per-tile (max, sum-exp), z_{i,y_i}, exp tile P
+//     logits GEMM (FWD_STATS_P)  exp tile P = bf16(exp(z - ref)), per half tile (ref, sum of
+//                                those exps), z_{i,y_i}
 //     combine                    lse_i, loss_i, alpha_i = exp(ref_i - lse_i), label entry of P,
 //                                Ht = alpha * H_c
-//     logits GEMM (FWD_GRAD)     only if a logit exceeded its reference by > 60 nats:
-//                                the exact gradient tile replaces P (alpha = 1)
+//     only if the chunk's guard is set (a 32-column sum of exp(z - ref) above ~e^60):
+//       logits GEMM (FWD_STATS)  exact online statistics
+//       combine                  again, with alpha = 1
+//       logits GEMM (FWD_GRAD)   the exact gradient tile replaces P
 //     backward GEMMs (one launch) dH_c = (g/n) alpha (P W) and dW (+)= (g/n) P^T Ht
 //   finalize                     loss = sum_i loss_i / n
 // lce_forward runs prepare, FWD_STATS + combine per chunk, finalize;
@@ -321,9 +324,9 @@ int logits_gemm(const Call& c, int64_t c0, int64_t rows, const LogitsArgs& a) {
   p.guard = a.guard;
   p.only_if = a.only_if;
   const double flops = 2.0 * static_cast<double>(rows) * static_cast<double>(ncols) * static_cast<double>(c.d);
-  int kind = K_LOGITS_STATS;
+  int kind = a.only_if ? K_OTHER : K_LOGITS_STATS;
   if (a.mode == lce::FWD_REF) kind = K_LOGITS_REF;
-  if (a.mode == lce::FWD_GRAD) kind = a.only_if ? K_OTHER : K_LOGITS_GRAD;
+  if (a.mode == lce::FWD_GRAD && !a.only_if) kind = K_LOGITS_GRAD;
   const int no_loads = (c.o.reserved == LCE_TEST_FORCE_TIMEOUT && a.mode == lce::FWD_STATS) ? 1 : 0;
   return timed(c.s, kind, a.only_if ? 0.0 : flops, [&] {
     return cuda_rc(lce::launch_logits(mA, mB, mC, rows, ncols, c.d, p, no_loads, c.dev.num_sms, c.s));
@@ -452,14 +455,27 @@ int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* l
 
   const double cbytes = static_cast<double>(rows) *
                         (16.0 * static_cast<double>(c.L.T) + 4 + 8 + 4 + 4 + 4 + 4 + 2 + 4.0 * static_cast<double>(c.d));
-  LCE_TRY(timed(c.s, K_COMBINE, cbytes, [&] {
-    return cuda_rc(lce::launch_combine_exp(
-        reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(2 * c.L.T), static_cast<int>(rows),
-        reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0, static_cast<int>(c.V), c.o.ignore_index, ref,
-        guard, lse + c0, loss_i + c0, alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp,
-        reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), static_cast<int>(c.d),
-        reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
-  }));
+  auto combine = [&](const int* only_if) {
+    return timed(c.s, only_if ? K_OTHER : K_COMBINE, only_if ? 0.0 : cbytes, [&] {
+      return cuda_rc(lce::launch_combine_exp(
+          reinterpret_cast<const float2*>(c.ws + c.L.partials), static_cast<int>(2 * c.L.T), static_cast<int>(rows),
+          reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0, static_cast<int>(c.V), c.o.ignore_index, ref,
+          guard, lse + c0, loss_i + c0, alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp,
+          reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), static_cast<int>(c.d),
+          reinterpret_cast<__nv_bfloat16*>(Ht), only_if, c.s));
+    });
+  };
+  LCE_TRY(combine(nullptr));
+
+  // If the guard is set (a logit far above its row reference), the statistics
+  // above may have overflowed: recompute them exactly (online max / sum-exp),
+  // combine again (alpha = 1), and write the exact gradient tile. All three
+  // launches return at once when the guard is clear.
+  LogitsArgs x;
+  x.mode = lce::FWD_STATS;
+  x.only_if = guard;
+  LCE_TRY(logits_gemm(c, c0, rows, x));
+  LCE_TRY(combine(guard));
 
   LogitsArgs g;
   g.mode = lce::FWD_GRAD;

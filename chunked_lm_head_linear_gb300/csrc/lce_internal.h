@@ -34,7 +34,7 @@ enum FwdMode : int {
 
 // An exp-tile entry may exceed the row reference by at most this many nats;
 // beyond it the chunk falls back to the exact gradient tile (FWD_GRAD).
-constexpr float kRefGuardNats = 60.f;
+constexpr float kRefGuardSum = 1.0e26f;  // ~e^60: bound on a 32-column sum of exp(z - ref)
 
 struct FwdParams {
   int mode;
@@ -99,11 +99,13 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
                            int V, long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
 // Per row of a chunk: lse, loss_i, alpha_i = exp(ref_i - lse_i) (1 if the chunk's guard is set,
 // 0 for ignored rows), the label entry of the exp tile P, and Ht_i = bf16(alpha_i H_i) for the
-// chunk's rows of H [rows, d] (the B operand of the dW GEMM).
+// chunk's rows of H [rows, d] (the B operand of the dW GEMM). With only_if, the launch does
+// nothing unless *only_if != 0.
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp,
-                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, cudaStream_t s);
+                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if,
+                               cudaStream_t s);
 // Vocabulary shards: per-row partial (max, sum-exp, target logit, has-target)
 // of this shard, and the fixed-order merge of R shards' partials.
 cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,

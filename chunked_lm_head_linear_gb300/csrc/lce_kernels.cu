@@ -25,10 +25,13 @@ constexpr float kLog2e = 1.4426950408889634f;
 // staging tile as TMA stores of 32 rows x 64 bf16.
 //   FWD_STATS:   per (row, 128-column half tile) max m and sum of exp(z - m)
 //                over the in-vocabulary columns, plus the label's logit.
-//   FWD_STATS_P: FWD_STATS, and the exp tile P = bf16(exp(z - ref_row)) for the
-//                backward, where ref_row is the row's maximum over the first
-//                128 words; sets the chunk's guard word if a logit exceeds
-//                ref_row by more than kRefGuardNats (bf16 range protection).
+//   FWD_STATS_P: the exp tile P = bf16(exp(z - ref_row)) for the backward,
+//                where ref_row is the row's maximum over the first 128 words,
+//                and per (row, half tile) the pair (ref_row, sum of those
+//                exps), plus the label's logit; sets the chunk's guard word if
+//                a 32-column sum exceeds kRefGuardSum (range protection: the
+//                chunk's statistics and gradient tile are then recomputed
+//                exactly by conditional launches).
 //   FWD_REF:     ref_row (launched for the first tile only; the warps holding
 //                columns 128..255 do nothing).
 //   FWD_GRAD:    the gradient tile exp(z - lse) - [v = y] in bf16 for valid
@@ -36,6 +39,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 // Columns past the vocabulary are masked to -inf (zero logits are not neutral
 // in a softmax); stores past the vocabulary are dropped by TMA.
 // ----------------------------------------------------------------------------
+// The label's logit if it lies in these 32 columns (yo = its column within
+// them). The branch is taken for about one group in 4700, so the unrolled
+// compares cost almost nothing.
+__device__ __forceinline__ void take_label(const float (&v)[32], int yo, float& zt, bool& have_t) {
+  if (yo >= 0 && yo < 32) {
+#pragma unroll
+    for (int c = 0; c < 32; ++c)
+      if (c == yo) {
+        zt = v[c];
+        have_t = true;
+      }
+  }
+}
+
 struct FwdEpi {
   using Params = FwdParams;
   struct State {};
@@ -86,6 +103,30 @@ struct FwdEpi {
           for (int c = 0; c < 32; ++c)
             if (c0 + c >= vlim) v[c] = -INFINITY;
         }
+        if (p.mode == FWD_STATS_P) {
+          // One exp per element: the exp tile's values exp(z - ref) also give the row's sum
+          // (partials against ref instead of the tile maximum). A 32-column sum above
+          // kRefGuardSum sets the guard (the chunk is then redone exactly).
+          float s2 = 0.f;
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float e0 = ex2_approx(fmaf(v[c], kLog2e, -rb));
+            const float e1 = ex2_approx(fmaf(v[c + 1], kLog2e, -rb));
+            s2 += e0;
+            s2 += e1;
+            pk[c / 2] = pack_bf16x2(e0, e1);
+          }
+          s += s2;
+          m = refv;
+          over |= !(s2 <= kRefGuardSum);
+          take_label(v, ycol - c0, zt, have_t);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<uint4*>(ctx.stage + stage_off(lane, hh * 4 + q)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          continue;
+        }
         if (stats || p.mode == FWD_REF) {
           float cm = v[0];
 #pragma unroll
@@ -102,13 +143,7 @@ struct FwdEpi {
 #pragma unroll
             for (int c = 0; c < 32; ++c) s2 += ex2_approx(fmaf(v[c], kLog2e, -mb));
             s += s2;
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c0 + c == ycol) {
-                zt = v[c];
-                have_t = true;
-              }
-            over |= cm > refv + kRefGuardNats;
+            take_label(v, ycol - c0, zt, have_t);
           }
         }
         if (store) {
@@ -331,7 +366,8 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
                                                      float* __restrict__ loss_i, float* __restrict__ alpha,
                                                      __nv_bfloat16* __restrict__ P, long long ldp,
                                                      const uint4* __restrict__ H, int groups_per_row,
-                                                     uint4* __restrict__ Ht) {
+                                                     uint4* __restrict__ Ht, const int* __restrict__ only_if) {
+  if (only_if != nullptr && *only_if == 0) return;  // conditional launch whose condition is false
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -738,13 +774,14 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp,
-                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, cudaStream_t s) {
+                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if,
+                               cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
   k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, ref, guard,
                                                        lse, loss_i, alpha, P, ldp, reinterpret_cast<const uint4*>(H),
-                                                       d / 8, reinterpret_cast<uint4*>(Ht));
+                                                       d / 8, reinterpret_cast<uint4*>(Ht), only_if);
   return cudaGetLastError();
 }
 

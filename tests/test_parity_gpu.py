@@ -126,10 +126,10 @@ def test_large_logits_and_zipf_labels(cuda_lib):
 
 
 def test_reference_guard_falls_back_to_exact_gradient(cuda_lib):
-    """The fused call stores exp(z - ref) with ref = the row's maximum over the
-    first 128 words. A word outside them whose logits reach ~80 sigma
-    above it trips the guard; the chunk must then use the exact gradient tile
-    and still match the oracle."""
+    """The fused call stores and sums exp(z - ref) with ref = the row's maximum
+    over the first 128 words. A word outside them whose logits reach ~80 sigma
+    above it overflows those sums and trips the guard; the chunk must then be
+    redone exactly (statistics, combine, gradient tile) and match the oracle."""
     inp = small_inputs(300, 64, 1000, seed=17, sigma_w=0.05)
     W = inputs.bf16_bits_to_f32(inp["W"]).astype(np.float64)
     W[700] = 10.0                                  # z_{i,700} = 10 * sum_k H_ik ~ N(0, 80^2)
