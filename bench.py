@@ -230,6 +230,9 @@ def main():
                          "--shards shards run in turn on one GPU (partial dH summed by torch in place of the "
                          "all-reduce)")
     ap.add_argument("--shards", type=int, default=4, help="with --path vshard: number of vocabulary shards")
+    ap.add_argument("--cublas-logits", action="store_true",
+                    help="also time cuBLAS (torch.matmul, bf16 output) on one chunk's logits GEMM, C x V x d, "
+                         "for comparison with the exp-tile pass; reported as cublas_logits_gemm")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -368,6 +371,29 @@ def main():
            "h2d_bytes_per_step": H_host.numel() * 2 + y_host.numel() * 8, "d2h_bytes_per_step": 4,
            "loss_last_step": float(loss_host.item())}
 
+    cublas = None
+    if args.cublas_logits:
+        C = chunk if chunk > 0 else N
+        out = torch.empty((C, V), dtype=torch.bfloat16, device=dev)
+        Hc = H[:C]
+        for _ in range(3):
+            torch.matmul(Hc, W.t(), out=out)
+        iters = max(10, args.steps)
+        barrier()
+        ev0.record(stream)
+        for _ in range(iters):
+            torch.matmul(Hc, W.t(), out=out)
+        ev1.record(stream)
+        barrier()
+        ms_c = ev0.elapsed_time(ev1) / iters
+        lg = prof.get("logits_stats", {})
+        ours = lg["ms"] / lg["launches"] if lg.get("launches") else None
+        cublas = {"shape": f"{C} x {V} x {d}", "ms": ms_c, "tflops": 2.0 * C * V * d / (ms_c * 1e-3) / 1e12,
+                  "exp_tile_pass_ms": ours,
+                  "note": "cuBLAS writes the bf16 logits; the exp-tile pass writes bf16 exp(z - ref) and the "
+                          "per-tile sums; both measured in this run, the cuBLAS loop after the fused steps"}
+        del out
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -419,6 +445,7 @@ def main():
         "peak_source": peak_src, "flops_per_step": flops_step,
         "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches, "e2e": e2e, "clocks": clk,
         **({"hbm_kernels": hbm_kernels} if hbm_kernels else {}),
+        **({"cublas_logits_gemm": cublas} if cublas else {}),
         "extra_device_bytes": int(ws.numel()), "unfused_logits_bytes": N * V * 4,
     }
     if world == 1 and not args.no_cpu_baseline:
