@@ -142,8 +142,11 @@ def cpu_baseline(inp, target_s=12.0, max_rows=4096):
         return time.perf_counter() - t0
 
     run(32)            # the first call pays one-time costs (allocation, BLAS start-up)
-    t32 = run(32)
-    rows = int(min(max_rows, inp["H"].shape[0], max(32, 32 * target_s / max(t32, 1e-3))))
+    t32, t96 = run(32), run(96)
+    # each call has a fixed part (writing the fp64 dW [V, d]) and a part per row
+    per_row = max((t96 - t32) / 64.0, 1e-6)
+    fixed = max(t32 - 32 * per_row, 0.0)
+    rows = int(min(max_rows, inp["H"].shape[0], max(32, (target_s - fixed) / per_row)))
     rows = max(32, rows // 32 * 32)
     t = run(rows)
     return {"value": rows / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
@@ -161,12 +164,17 @@ def run_reference(args, w):
     Hd = oracle.decode_bf16(inp["H"])
     Wd = oracle.decode_bf16(inp["W"])
     y = inp["y"]
-    oracle.lce_f64(Hd[:16], Wd, y[:16])          # first call pays page faults: calibrate on a warm one
-    t16 = time.perf_counter()
-    oracle.lce_f64(Hd[:16], Wd, y[:16])
-    t16 = time.perf_counter() - t16
+    def timed_call(rows):
+        t = time.perf_counter()
+        oracle.lce_f64(Hd[:rows], Wd, y[:rows])
+        return time.perf_counter() - t
+
+    timed_call(16)                               # first call pays page faults: calibrate on warm ones
+    t16, t80 = timed_call(16), timed_call(80)
+    per_row = max((t80 - t16) / 64.0, 1e-6)      # each call: a fixed part (the fp64 dW) + a part per row
+    fixed = max(t16 - 16 * per_row, 0.0)
     budget = 150.0 / max(1, args.steps + args.warmup)     # whole run within a few minutes
-    rows = int(max(16, min(w.N, 16 * budget / max(t16, 1e-3))) // 16 * 16)
+    rows = int(max(16, min(w.N, (budget - fixed) / per_row)) // 16 * 16)
     for s in range(args.warmup):
         oracle.lce_f64(Hd[:rows], Wd, y[:rows])
     t0 = time.perf_counter()

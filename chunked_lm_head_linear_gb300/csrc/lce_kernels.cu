@@ -729,9 +729,9 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
   if (P <= 0) return cudaSuccess;
   // Balance: every cluster should end with the same share of the launch's time. A dH k-block (A
-  // K-major, B N-major) runs in ~0.93 of a dW k-block's time (both N-major): 637 vs 685 SM cycles
+  // K-major, B N-major) runs in ~0.98 of a dW k-block's time (both N-major): 584 vs 594 SM cycles
   // per 64-deep k-block, measured on the Qwen3.5-2B-like head with cycle counters in the MMA issuer.
-  constexpr double kDhKblockCost = 0.93;
+  constexpr double kDhKblockCost = 0.98;
   const double h_cost = kDhKblockCost * p.h_k, w_cost = p.w_k;
   const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
   const long long hmax = (nH + P - 1) / P;
