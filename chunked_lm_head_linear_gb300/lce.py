@@ -6,9 +6,14 @@ library's CUDA kernels. There is no CPU fallback: if the library is missing,
 ``load()`` raises.
 
 Entry points (same names as the C ABI):
-  lce_forward(H, W, y)              -> loss [1], lse [N]
-  lce_backward(H, W, y, lse, g)     -> dH [N, d] bf16, dW [V, d] fp32
-  lce_fwd_bwd(H, W, y, g)           -> loss, lse, dH, dW
+  lce_forward(H, W, y)                   -> loss [1], lse [N]
+  lce_backward(H, W, y, lse, g)          -> dH [N, d] bf16, dW [V, d] fp32
+  lce_fwd_bwd(H, W, y, g)                -> loss, lse, dH, dW
+  lce_fwd_bwd_sliced(H, W, y, bounds=..) -> the same, dW finished in vocabulary slices with an event each
+  lce_forward_noalloc(H, W, y)           -> loss, lse without a workspace
+  lce_vshard_forward_stats / lce_vshard_combine / lce_vshard_backward   W split by vocabulary rows
+  lce_rmsnorm_forward / lce_rmsnorm_backward / lce_norm_fwd_bwd         the final RMSNorm, alone or fused
+  lce_scale_grads, auto_chunk (lce_auto_chunk), workspace_size, read_device_status, profile_begin/end
 """
 from __future__ import annotations
 
@@ -302,6 +307,29 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
     return loss, lse, dH, dW
 
 
+def lce_forward_noalloc(H, W, y, *, loss=None, lse=None, stream=None, **opt_kw):
+    """loss and lse like lce_forward, but the library uses its fixed device
+    scratch array instead of a workspace (nothing is allocated by the library;
+    ``loss`` / ``lse`` may be passed in so that this call allocates nothing
+    either). Calls that overlap on the GPU share the scratch and must be
+    serialised by the caller."""
+    import torch
+    N, d, V = _check_inputs(H, W, y)
+    _check_dev(loss, "loss", torch.float32, numel=1, device=H.device)
+    _check_dev(lse, "lse", torch.float32, numel=N, device=H.device)
+    if "chunk_tokens" in opt_kw and opt_kw["chunk_tokens"] == "auto":
+        raise ValueError('lce_forward_noalloc: chunk_tokens="auto" sizes a workspace; give a number')
+    opts = make_opts(**opt_kw)
+    if loss is None:
+        loss = torch.empty(1, dtype=torch.float32, device=H.device)
+    if lse is None:
+        lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
+    rc = load().lce_forward_noalloc(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(loss), _ptr(lse), ctypes.byref(opts),
+                                    _stream(stream))
+    _raise(rc, "lce_forward_noalloc")
+    return loss, lse
+
+
 LCE_MAX_SLICES = 4096
 LCE_SLICE_ALIGN = 256
 
@@ -377,6 +405,49 @@ def profile_end() -> dict:
         name = load().lce_kernel_name(k).decode()
         out[name] = {"launches": p.launches[k], "ms": p.ms[k], "work": p.work[k]}
     return out
+
+
+# The C ABI's helper calls under their own names (the wrappers above use shorter ones).
+def lce_opts_init(**opt_kw) -> LceOpts:
+    """Defaults of the C ABI (chunk chosen by the library, ignore_index -100,
+    mean), then the given fields."""
+    return make_opts(**opt_kw)
+
+
+def lce_workspace_size(op: int, N: int, d: int, V: int, opts: LceOpts | None = None) -> int:
+    return workspace_size(op, N, d, V, opts)
+
+
+def lce_auto_chunk(N: int, d: int, V: int, budget_bytes: int, opts: LceOpts | None = None) -> int:
+    return auto_chunk(N, d, V, budget_bytes, opts)
+
+
+def lce_read_device_status(workspace, stream=None) -> int:
+    return read_device_status(workspace, stream)
+
+
+def lce_status_string(code: int) -> str:
+    return status_string(code)
+
+
+def lce_version() -> int:
+    return int(load().lce_version())
+
+
+def lce_profile_begin():
+    profile_begin()
+
+
+def lce_profile_end() -> dict:
+    return profile_end()
+
+
+def lce_kernel_name(kind: int) -> str:
+    return load().lce_kernel_name(int(kind)).decode()
+
+
+def lce_rmsnorm_workspace_size(N: int, d: int) -> int:
+    return int(load().lce_rmsnorm_workspace_size(int(N), int(d)))
 
 
 # ---------------------------------------------------------------------------

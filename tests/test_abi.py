@@ -29,6 +29,12 @@ def test_header_and_binding_agree():
     assert _declared_functions() == sorted(lce.EXPORTED)
 
 
+def test_binding_has_every_entry_point_by_name():
+    """The Python binding offers each C entry point under the same name."""
+    for name in lce.EXPORTED:
+        assert callable(getattr(lce, name, None)), name
+
+
 def test_every_declared_symbol_is_exported(lib):
     for name in _declared_functions():
         assert hasattr(lib, name), name

@@ -60,6 +60,19 @@ def test_noalloc_forward_matches_workspace_forward_twice(cuda_lib):
         assert rel <= TOL_LSE
 
 
+def test_noalloc_binding_writes_into_caller_tensors(cuda_lib):
+    """The Python binding of the same name, with caller-owned outputs."""
+    import torch
+    H, W, y = _case(4, N=300, d=128, V=1000)
+    ref_loss, ref_lse = cuda_lib.lce_forward(H, W, y, sync_check=True)
+    loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    lse = torch.full((300,), float("nan"), dtype=torch.float32, device="cuda")
+    out = cuda_lib.lce_forward_noalloc(H, W, y, loss=loss, lse=lse, sync_check=True)
+    assert out[0] is loss and out[1] is lse
+    assert abs(loss.item() - ref_loss.item()) <= TOL_LOSS * abs(ref_loss.item())
+    assert ((lse - ref_lse).abs() / ref_lse.abs().clamp_min(1.0)).max().item() <= TOL_LSE
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     lib = cuda_lib.load()
     H, W, y = _case(3, N=256, d=64, V=4096)
