@@ -202,7 +202,9 @@ def config_of(w, chunk, args):
         cfg["path"] = args.path
         if args.path == "vshard":
             cfg["vocab_shards"] = args.shards
-            cfg["flops_executed_per_token"] = "8*V*d (logits recomputed in the shard backward)"
+            cfg["vshard_method"] = args.vshard_method
+            cfg["flops_executed_per_token"] = ("6*V*d (exp tile kept per chunk)" if args.vshard_method == "stored"
+                                               else "8*V*d (logits recomputed in the shard backward)")
         if args.path == "norm":
             cfg["norm"] = "zero-centred RMSNorm of x [N, d] in front of the head (eps 1e-6)"
     if getattr(args, "slices", 0) > 0:
@@ -238,6 +240,9 @@ def main():
                          "--shards shards run in turn on one GPU (partial dH summed by torch in place of the "
                          "all-reduce)")
     ap.add_argument("--shards", type=int, default=4, help="with --path vshard: number of vocabulary shards")
+    ap.add_argument("--vshard-method", default="stored", choices=["stored", "recompute"],
+                    help="with --path vshard: the per-chunk calls keeping the exp tile (lce_vshard_chunk_*), or the "
+                         "three calls that recompute the logits in the backward")
     ap.add_argument("--cublas-logits", action="store_true",
                     help="also time cuBLAS (torch.matmul, bf16 output) on one chunk's logits GEMM, C x V x d, "
                          "for comparison with the exp-tile pass; reported as cublas_logits_gemm")
@@ -294,11 +299,34 @@ def main():
         ws_norm = torch.empty(lce.workspace_size(lce.LCE_OP_NORM_FWD_BWD, N, d, V, lce.make_opts(**opts)),
                               dtype=torch.uint8, device=dev)
     shard_cuts = [V * r // args.shards // 8 * 8 for r in range(args.shards)] + [V]
+    if args.path == "vshard" and args.vshard_method == "stored":
+        vs_chunk = max(1, min(chunk or 4096, N))
+        vs_ws = [lce.vshard_chunk_workspace(H, W[shard_cuts[r]:shard_cuts[r + 1]], y, chunk_tokens=vs_chunk)
+                 for r in range(args.shards)]
+        vs_dH = [torch.empty((N, d), dtype=torch.float32, device=dev) for _ in range(args.shards)]
 
     def step(Hx, yx):
         if args.path == "norm":
             loss, _, dx, _, _ = lce.lce_norm_fwd_bwd(Hx, w_norm, W, yx, dW=dW, workspace=ws_norm, **opts)
             return loss, dx
+        if args.path == "vshard" and args.vshard_method == "stored":
+            cuts = shard_cuts
+            per_chunk = []
+            for c0 in range(0, N, vs_chunk):
+                rows = min(vs_chunk, N - c0)
+                st = torch.stack([lce.lce_vshard_chunk_stats(Hx, W[cuts[r]:cuts[r + 1]], yx, cuts[r], V, c0, rows,
+                                                             workspace=vs_ws[r], chunk_tokens=vs_chunk)
+                                  for r in range(args.shards)])
+                for r in range(args.shards):
+                    lce.lce_vshard_chunk_backward(Hx, W[cuts[r]:cuts[r + 1]], yx, cuts[r], V, c0, rows, st,
+                                                  workspace=vs_ws[r], lse=lse, dH_partial=vs_dH[r],
+                                                  dW_shard=dW[cuts[r]:cuts[r + 1]], chunk_tokens=vs_chunk)
+                per_chunk.append(st)
+            loss, _ = lce.lce_vshard_combine(torch.cat(per_chunk, dim=1), yx, V)
+            dH = vs_dH[0]
+            for r in range(1, args.shards):
+                dH.add_(vs_dH[r])
+            return loss, dH
         if args.path == "vshard":
             cuts = shard_cuts
             stats = [lce.lce_vshard_forward_stats(Hx, W[cuts[r]:cuts[r + 1]], yx, cuts[r], V, chunk_tokens=chunk)

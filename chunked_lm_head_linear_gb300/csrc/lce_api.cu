@@ -92,6 +92,18 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
     return at;
   };
   L.status = take(sizeof(DevStatus));
+  if (op == LCE_OP_VSHARD_CHUNK) {  // one chunk: its exp tile, statistics, references, alpha and Ht
+    L.chunks = 1;
+    L.ztgt = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.partials = take(sizeof(float) * 2 * static_cast<size_t>(L.C) * static_cast<size_t>(2 * L.T));
+    L.ref = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.alpha = take(sizeof(float) * static_cast<size_t>(L.C));
+    L.guard = take(sizeof(int));
+    L.Ht = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(d));
+    L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
+    L.total = off;
+    return L;
+  }
   if (op == LCE_OP_VSHARD_COMBINE) {
     L.loss_i = take(sizeof(float) * static_cast<size_t>(N > 0 ? N : 1));
     L.total = off;
@@ -497,9 +509,9 @@ int row_references(const Call& c) {
   return logits_gemm(c, 0, c.N, a);
 }
 
-int prepare(const Call& c, const float* grad_loss) {
+int prepare(const Call& c, const float* grad_loss, bool reset_guards = true) {
   int* guards = c.L.guard ? reinterpret_cast<int*>(c.ws + c.L.guard) : nullptr;
-  const int nguards = c.L.guard ? static_cast<int>(c.L.chunks) : 0;
+  const int nguards = c.L.guard && reset_guards ? static_cast<int>(c.L.chunks) : 0;
   return timed(c.s, K_PREPARE, 8.0 * static_cast<double>(c.N), [&] {
     return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V_total), c.o.ignore_index, c.o.reduction,
                                        c.o.n_valid_override, grad_loss, c.st, guards, nguards, c.s));
@@ -562,7 +574,7 @@ size_t lce_workspace_size(int op, int64_t N, int64_t d, int64_t V, const lce_opt
   lce_opts o;
   lce_opts_init(&o);
   if (opts) o = *opts;
-  if (op < LCE_OP_FORWARD || op > LCE_OP_NORM_FWD_BWD) return 0;
+  if (op < LCE_OP_FORWARD || op > LCE_OP_VSHARD_CHUNK) return 0;
   if (check_sizes(N, d, V, &o) != LCE_OK) return 0;
   if (op == LCE_OP_NORM_FWD_BWD) return norm_layout(N, d, V, &o).total;
   return make_layout(op, N, d, V, &o).total;
@@ -775,6 +787,91 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
     const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
     LCE_TRY(backward_chunk(c, c0, rows, lse, dH_partial, dW_shard, c.o.accumulate_dW || c0 > 0, true));
   }
+  return finish(c);
+}
+
+// Checks shared by the two per-chunk shard calls; fills the call record.
+static int vshard_chunk_begin(Call* c, const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                              int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t c0, int64_t rows,
+                              const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  LCE_TRY(begin(c, LCE_OP_VSHARD_CHUNK, H, W_shard, y, N, d, V_shard, opts, ws, ws_bytes, stream));
+  LCE_TRY(shard_args(V_shard, vocab_offset, V_total));
+  if (c->o.reserved != 0 || c0 < 0 || rows < 0 || c0 > N - rows || rows > c->L.C) return LCE_ERR_INVALID_ARG;
+  c->V_total = V_total;
+  c->y_offset = vocab_offset;
+  return LCE_OK;
+}
+
+int lce_vshard_chunk_stats(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                           int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t c0, int64_t rows,
+                           float* stats, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream) {
+  Call c;
+  LCE_TRY(vshard_chunk_begin(&c, H, W_shard, y, N, d, V_shard, vocab_offset, V_total, c0, rows, opts, ws, ws_bytes,
+                             stream));
+  if (rows > 0 && !stats) return LCE_ERR_INVALID_ARG;
+  if (stats && !aligned(stats, 16)) return LCE_ERR_ALIGNMENT;
+  if (rows == 0) return LCE_OK;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, nullptr));  // also clears the chunk's guard word
+  float* ref = reinterpret_cast<float*>(c.ws + c.L.ref);
+  LogitsArgs r;
+  r.mode = lce::FWD_REF;
+  r.ref = ref;
+  LCE_TRY(logits_gemm(c, c0, rows, r));
+  LogitsArgs a;
+  a.mode = lce::FWD_STATS_PX;
+  a.ref = ref;
+  a.P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
+  a.guard = reinterpret_cast<int*>(c.ws + c.L.guard);
+  LCE_TRY(logits_gemm(c, c0, rows, a));
+  const double bytes = static_cast<double>(rows) * (16.0 * static_cast<double>(c.L.T) + 8 + 4 + 16);
+  LCE_TRY(timed(c.s, K_COMBINE, bytes, [&] {
+    return cuda_rc(lce::launch_shard_stats(reinterpret_cast<const float2*>(c.ws + c.L.partials),
+                                           static_cast<int>(2 * c.L.T), static_cast<int>(rows),
+                                           reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0, vocab_offset,
+                                           static_cast<int>(V_shard), static_cast<int>(V_total), c.o.ignore_index,
+                                           reinterpret_cast<float4*>(stats), c.s));
+  }));
+  return finish(c);
+}
+
+int lce_vshard_chunk_backward(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                              int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t c0, int64_t rows,
+                              const float* stats_all, int64_t R, const float* grad_loss, float* lse,
+                              float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
+                              void* stream) {
+  Call c;
+  LCE_TRY(vshard_chunk_begin(&c, H, W_shard, y, N, d, V_shard, vocab_offset, V_total, c0, rows, opts, ws, ws_bytes,
+                             stream));
+  if (R < 1 || R > 4096 || !dW_shard || (rows > 0 && (!stats_all || !lse || !dH_partial))) return LCE_ERR_INVALID_ARG;
+  if (!aligned(dW_shard, 16) || (stats_all && !aligned(stats_all, 16)) || (lse && !aligned(lse, 4)) ||
+      (dH_partial && !aligned(dH_partial, 16)) || (grad_loss && !aligned(grad_loss, 4)))
+    return LCE_ERR_ALIGNMENT;
+  if (rows == 0) return LCE_OK;
+  LCE_TRY(device_check(&c.dev));
+  LCE_TRY(prepare(c, grad_loss, false));  // n and g/n over all N labels; keeps the guard of the stats call
+  float* alpha = reinterpret_cast<float*>(c.ws + c.L.alpha);
+  int* guard = reinterpret_cast<int*>(c.ws + c.L.guard);
+  uint16_t* P = reinterpret_cast<uint16_t*>(c.ws + c.L.P);
+  uint16_t* Ht = reinterpret_cast<uint16_t*>(c.ws + c.L.Ht);
+  const double sbytes = static_cast<double>(rows) * (16.0 * static_cast<double>(R) + 8 + 4 + 4 + 4 + 2 +
+                                                     4.0 * static_cast<double>(d));
+  LCE_TRY(timed(c.s, K_COMBINE, sbytes, [&] {
+    return cuda_rc(lce::launch_vshard_scale(
+        reinterpret_cast<const float4*>(stats_all), static_cast<int>(R), static_cast<int>(rows), c.y + c0,
+        vocab_offset, static_cast<int>(V_shard), static_cast<int>(V_total), c.o.ignore_index,
+        reinterpret_cast<const float*>(c.ws + c.L.ref), guard, lse + c0, alpha,
+        reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp, reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * d),
+        static_cast<int>(d), reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
+  }));
+  // The exact gradient tile, only if the stats call found the exp tile out of range.
+  LogitsArgs g;
+  g.mode = lce::FWD_GRAD;
+  g.lse_rows = lse + c0;
+  g.P = P;
+  g.only_if = guard;
+  LCE_TRY(logits_gemm(c, c0, rows, g));
+  LCE_TRY(dh_dw(c, c0, rows, alpha, Ht, dH_partial, dW_shard, c.o.accumulate_dW || c0 > 0, true));
   return finish(c);
 }
 

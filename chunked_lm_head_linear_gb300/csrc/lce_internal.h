@@ -30,11 +30,14 @@ enum FwdMode : int {
   FWD_STATS_P = 1,  // FWD_STATS + exp-tile P = bf16(exp(z - ref_row)) stored for the backward
   FWD_GRAD = 2,     // gradient tile exp(z - lse) - onehot (valid rows), from a known lse
   FWD_REF = 3,      // row maximum over the first 128 words (one launch over the first tile)
+  FWD_STATS_PX = 4, // exact FWD_STATS partials + the exp tile P = bf16(exp(z - ref_row)) (vocabulary shards:
+                    // the statistics are exchanged before the tile's scale is known)
 };
 
 // An exp-tile entry may exceed the row reference by at most this many nats;
 // beyond it the chunk falls back to the exact gradient tile (FWD_GRAD).
 constexpr float kRefGuardSum = 1.0e26f;  // ~e^60: bound on a 32-column sum of exp(z - ref)
+constexpr float kRefGuardLogit = 60.f;   // the same bound in nats, on lse - ref (vocabulary shards)
 
 struct FwdParams {
   int mode;
@@ -47,12 +50,12 @@ struct FwdParams {
   const int64_t* y;      // labels of this chunk
   float2* partials;      // [rows, nparts] (max, sum-exp) per 128-column half tile
   float* ztgt;           // [rows] logit of the label
-  float* ref;            // [rows] row reference (FWD_REF output, FWD_STATS_P input)
+  float* ref;            // [rows] row reference (FWD_REF output, FWD_STATS_P / FWD_STATS_PX input)
   const float* lse;      // [rows] (FWD_GRAD input)
   __nv_bfloat16* P;      // [rows, ldp] exp tile (FWD_STATS_P) or gradient tile (FWD_GRAD)
   long long ldp;
   int* flags;
-  int* guard;            // FWD_STATS_P: set to 1 if some logit exceeds its row reference + guard
+  int* guard;            // FWD_STATS_P(X): set to 1 if some logit exceeds its row reference + guard
   const int* only_if;    // if non-null, the launch does nothing unless *only_if != 0
 };
 
@@ -113,6 +116,17 @@ cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, con
                                cudaStream_t s);
 cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const int64_t* y, int V_total,
                                long long ignore_index, float* lse, float* loss_i, cudaStream_t s);
+// Chunk rows of the stored-tile vocabulary-parallel backward (two launches):
+// the merge of launch_shard_merge on stats [R, rows, 4] -> lse, setting *guard
+// for a row whose label lies in the shard and whose lse exceeds its reference
+// by more than kRefGuardLogit; then alpha_i = exp(ref_i - lse_i) (1 if *guard:
+// the tile is then the exact gradient; 0 for ignored rows), the label entry of
+// this shard's exp tile P when the label lies in the shard, and
+// Ht_i = bf16(alpha_i H_i) for H [rows, d].
+cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int64_t* y, long long y_offset,
+                                int V_shard, int V_total, long long ignore_index, const float* ref, int* guard,
+                                float* lse, float* alpha, __nv_bfloat16* P, long long ldp, const __nv_bfloat16* H,
+                                int d, __nv_bfloat16* Ht, cudaStream_t s);
 // Final zero-centred RMSNorm (lce_rmsnorm.cu). rmsnorm_bwd_blocks(N) partial
 // rows of d floats are the backward's scratch.
 int rmsnorm_bwd_blocks(long long N);

@@ -32,6 +32,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 //                a 32-column sum exceeds kRefGuardSum (range protection: the
 //                chunk's statistics and gradient tile are then recomputed
 //                exactly by conditional launches).
+//   FWD_STATS_PX: FWD_STATS's exact partials and FWD_STATS_P's exp tile (two
+//                exps per element), guard as FWD_STATS_P but on the tile only:
+//                the statistics stay exact (vocabulary shards exchange them
+//                before the tile's scale is known).
 //   FWD_REF:     ref_row (launched for the first tile only; the warps holding
 //                columns 128..255 do nothing).
 //   FWD_GRAD:    the gradient tile exp(z - lse) - [v = y] in bf16 for valid
@@ -79,9 +83,10 @@ struct FwdEpi {
       return;
     }
     const bool grad = p.mode == FWD_GRAD;
-    const bool stats = p.mode == FWD_STATS || p.mode == FWD_STATS_P;
-    const bool store = p.mode == FWD_STATS_P || grad;
-    const float refv = !live ? 0.f : (grad ? p.lse[r] : (p.mode == FWD_STATS_P ? p.ref[r] : 0.f));
+    const bool stats = p.mode == FWD_STATS || p.mode == FWD_STATS_P || p.mode == FWD_STATS_PX;
+    const bool store = p.mode == FWD_STATS_P || p.mode == FWD_STATS_PX || grad;
+    const bool by_ref = p.mode == FWD_STATS_P || p.mode == FWD_STATS_PX;  // the tile is exp(z - ref)
+    const float refv = !live ? 0.f : (grad ? p.lse[r] : (by_ref ? p.ref[r] : 0.f));
     const float rb = refv * kLog2e;
     const float gmask = (grad && !valid) ? 0.f : 1.f;   // gradient rows of ignored tokens are zero
 
@@ -148,6 +153,7 @@ struct FwdEpi {
         }
         if (store) {
           uint32_t pk[16];
+          float s3 = 0.f;
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             float e0 = ex2_approx(fmaf(v[c], kLog2e, -rb));
@@ -156,8 +162,11 @@ struct FwdEpi {
               e0 = (e0 - (c0 + c == ycol ? 1.f : 0.f)) * gmask;
               e1 = (e1 - (c0 + c + 1 == ycol ? 1.f : 0.f)) * gmask;
             }
+            s3 += e0;
+            s3 += e1;
             pk[c / 2] = pack_bf16x2(e0, e1);
           }
+          if (p.mode == FWD_STATS_PX) over |= !(s3 <= kRefGuardSum);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             *reinterpret_cast<uint4*>(ctx.stage + stage_off(lane, hh * 4 + q)) =
@@ -174,7 +183,7 @@ struct FwdEpi {
     if (stats) {
       p.partials[static_cast<long long>(r) * p.nparts + part] = make_float2(m, s);
       if (have_t) p.ztgt[r] = zt;
-      if (p.mode == FWD_STATS_P && over) *p.guard = 1;
+      if (by_ref && over) *p.guard = 1;
     }
   }
 };
@@ -344,7 +353,6 @@ __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ part
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
     merge_ms(m, s, m2, s2);
   }
-  float a = 0.f;  // alpha_i, decided by lane 0
   if (lane == 0) {
     const float l = m + logf(s);
     lse[r] = l;
@@ -470,6 +478,88 @@ __global__ void __launch_bounds__(256) k_shard_merge(const float4* __restrict__ 
   const long long yr = y[i];
   const bool valid = yr != ignore_index && yr >= 0 && yr < V_total;
   loss_i[i] = valid ? l - zt : 0.f;
+}
+
+// Stored-tile vocabulary-parallel backward, first pass, one thread per chunk
+// row: the merge of k_shard_merge over the R shards' statistics (stats
+// [R, rows, 4]) -> lse. A valid row whose label lies in this shard and whose
+// lse exceeds the shard's row reference by more than kRefGuardLogit sets the
+// chunk's guard: its label entry exp(z_y - ref) - exp(lse - ref) would leave
+// the fp32 range (and alpha = exp(ref - lse) underflow), so the chunk takes
+// the exact gradient tile instead.
+__global__ void __launch_bounds__(256) k_vshard_lse(const float4* __restrict__ stats, int R, int rows,
+                                                    const int64_t* __restrict__ y, long long y_offset, int V_shard,
+                                                    int V_total, long long ignore_index, const float* __restrict__ ref,
+                                                    int* __restrict__ guard, float* __restrict__ lse) {
+  const int r = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
+  if (r >= rows) return;
+  float M = -INFINITY;
+  for (int k = 0; k < R; ++k) M = fmaxf(M, stats[static_cast<long long>(k) * rows + r].x);
+  float S = 0.f;
+  for (int k = 0; k < R; ++k) {
+    const float4 q = stats[static_cast<long long>(k) * rows + r];
+    if (q.y > 0.f) S += q.y * exp2f((q.x - M) * kLog2e);
+  }
+  const float l = M + logf(S);
+  lse[r] = l;
+  const long long yr = y[r];
+  const bool valid = yr != ignore_index && yr >= 0 && yr < V_total;
+  const long long col = yr - y_offset;
+  if (valid && col >= 0 && col < V_shard && !(l - ref[r] <= kRefGuardLogit)) *guard = 1;
+}
+
+// Second pass, one warp per chunk row: alpha_i = exp(ref_i - lse_i) scales
+// this shard's exp tile exp(z - ref) into softmax probabilities (1 if the
+// chunk's guard is set, the tile then being the exact gradient; 0 for ignored
+// rows); the label's entry of the tile becomes exp(z_y - ref) - exp(lse - ref)
+// when the label lies in this shard, so that alpha P is softmax - onehot
+// there; Ht_i = bf16(alpha_i H_i).
+__global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__ stats, int R, int rows,
+                                                      const int64_t* __restrict__ y, long long y_offset, int V_shard,
+                                                      int V_total, long long ignore_index, const float* __restrict__ ref,
+                                                      const int* __restrict__ guard, const float* __restrict__ lse,
+                                                      float* __restrict__ alpha, __nv_bfloat16* __restrict__ P,
+                                                      long long ldp, const uint4* __restrict__ H, int groups_per_row,
+                                                      uint4* __restrict__ Ht) {
+  const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= rows) return;
+  float a = 0.f;
+  if (lane == 0) {
+    const long long yr = y[r];
+    const bool valid = yr != ignore_index && yr >= 0 && yr < V_total;
+    if (valid) {
+      if (*guard != 0) {
+        a = 1.f;
+      } else {
+        const float l = lse[r], rf = ref[r];
+        a = exp2f((rf - l) * kLog2e);
+        const long long col = yr - y_offset;
+        if (col >= 0 && col < V_shard) {
+          float zt = 0.f;  // the label's logit, from the shard that holds it (this one)
+          for (int k = 0; k < R; ++k) {
+            const float4 q = stats[static_cast<long long>(k) * rows + r];
+            zt += q.w > 0.f ? q.z : 0.f;
+          }
+          P[static_cast<long long>(r) * ldp + col] =
+              __float2bfloat16_rn(exp2f((zt - rf) * kLog2e) - exp2f((l - rf) * kLog2e));
+        }
+      }
+    }
+    alpha[r] = a;
+  }
+  a = __shfl_sync(0xffffffffu, a, 0);
+  const uint4* hr = H + static_cast<long long>(r) * groups_per_row;
+  uint4* tr = Ht + static_cast<long long>(r) * groups_per_row;
+  for (int g = lane; g < groups_per_row; g += 32) {
+    const uint4 h = hr[g];
+    const uint32_t w[4] = {h.x, h.y, h.z, h.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      o[q] = pack_bf16x2(__uint_as_float(w[q] << 16) * a, __uint_as_float(w[q] & 0xffff0000u) * a);
+    tr[g] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // x *= g in place for bf16 (8 per thread) and fp32 (4 per thread) arrays;
@@ -819,6 +909,21 @@ cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const in
   if (N <= 0) return cudaSuccess;
   const long long grid = (N + 255) / 256;
   k_shard_merge<<<static_cast<unsigned>(grid), 256, 0, s>>>(stats, R, N, y, V_total, ignore_index, lse, loss_i);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int64_t* y, long long y_offset,
+                                int V_shard, int V_total, long long ignore_index, const float* ref, int* guard,
+                                float* lse, float* alpha, __nv_bfloat16* P, long long ldp, const __nv_bfloat16* H,
+                                int d, __nv_bfloat16* Ht, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  k_vshard_lse<<<(rows + 255) / 256, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
+                                                  guard, lse);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  k_vshard_scale<<<(rows + 7) / 8, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
+                                                guard, lse, alpha, P, ldp, reinterpret_cast<const uint4*>(H), d / 8,
+                                                reinterpret_cast<uint4*>(Ht));
   return cudaGetLastError();
 }
 

@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
   lce_fwd_bwd_sliced(H, W, y, bounds=..) -> the same, dW finished in vocabulary slices with an event each
   lce_forward_noalloc(H, W, y)           -> loss, lse without a workspace
   lce_vshard_forward_stats / lce_vshard_combine / lce_vshard_backward   W split by vocabulary rows
+  lce_vshard_chunk_stats / lce_vshard_chunk_backward   the same per chunk, the exp tile kept between them
   lce_rmsnorm_forward / lce_rmsnorm_backward / lce_norm_fwd_bwd         the final RMSNorm, alone or fused
   lce_scale_grads, auto_chunk (lce_auto_chunk), workspace_size, read_device_status, profile_begin/end
 """
@@ -35,6 +36,7 @@ LCE_ERR_TIMEOUT = 7
 
 LCE_MEAN, LCE_SUM = 0, 1
 LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD, LCE_OP_VSHARD_COMBINE, LCE_OP_NORM_FWD_BWD = 0, 1, 2, 3, 4
+LCE_OP_VSHARD_CHUNK = 5
 LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
 LCE_TEST_FORCE_TIMEOUT = 0x7E57
 
@@ -44,7 +46,7 @@ EXPORTED = ("lce_opts_init", "lce_workspace_size", "lce_forward", "lce_backward"
             "lce_profile_end", "lce_kernel_name", "lce_forward_noalloc", "lce_auto_chunk",
             "lce_vshard_forward_stats", "lce_vshard_combine", "lce_vshard_backward",
             "lce_rmsnorm_workspace_size", "lce_rmsnorm_forward", "lce_rmsnorm_backward", "lce_norm_fwd_bwd",
-            "lce_scale_grads", "lce_fwd_bwd_sliced")
+            "lce_scale_grads", "lce_fwd_bwd_sliced", "lce_vshard_chunk_stats", "lce_vshard_chunk_backward")
 LCE_KERNEL_KINDS = 11
 # Kernel kinds whose profiled work is flops (tensor-core GEMMs); the others count bytes.
 GEMM_KINDS = ("logits_stats", "logits_grad", "gemm_dH_dW", "logits_ref")
@@ -116,6 +118,12 @@ def load(path: str | None = None):
         lib.lce_vshard_combine.restype = I32
         lib.lce_vshard_backward.argtypes = [P, P, P, I64, I64, I64, I64, I64, P, P, P, P, OPT, P, ctypes.c_size_t, P]
         lib.lce_vshard_backward.restype = I32
+        lib.lce_vshard_chunk_stats.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, I64, P, OPT, P, ctypes.c_size_t,
+                                               P]
+        lib.lce_vshard_chunk_stats.restype = I32
+        lib.lce_vshard_chunk_backward.argtypes = [P, P, P, I64, I64, I64, I64, I64, I64, I64, P, I64, P, P, P, P, OPT,
+                                                  P, ctypes.c_size_t, P]
+        lib.lce_vshard_chunk_backward.restype = I32
         F32 = ctypes.c_float
         lib.lce_rmsnorm_workspace_size.argtypes = [I64, I64]
         lib.lce_rmsnorm_workspace_size.restype = ctypes.c_size_t
@@ -507,6 +515,59 @@ def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, gra
                                     ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_backward")
     return dH, dW
+
+
+def vshard_chunk_workspace(H, W_shard, y, **opt_kw):
+    """Workspace for lce_vshard_chunk_stats / lce_vshard_chunk_backward (one chunk's exp tile)."""
+    N, d, Vs = _check_inputs(H, W_shard, y)
+    return _workspace(LCE_OP_VSHARD_CHUNK, N, d, Vs, make_opts(**opt_kw), H.device)
+
+
+def _chunk_ws(workspace, N, d, Vs, opts, device):
+    import torch
+    _check_dev(workspace, "workspace", torch.uint8, device=device)
+    if workspace is None or workspace.numel() < workspace_size(LCE_OP_VSHARD_CHUNK, N, d, Vs, opts):
+        raise LCEError(LCE_ERR_WORKSPACE, "vshard chunk calls need vshard_chunk_workspace(...)")
+    return workspace
+
+
+def lce_vshard_chunk_stats(H, W_shard, y, vocab_offset: int, V_total: int, c0: int, rows: int, *, workspace,
+                           stream=None, **opt_kw):
+    """Statistics [rows, 4] of chunk rows [c0, c0 + rows) of this shard (as
+    lce_vshard_forward_stats); the chunk's exp tile stays in ``workspace``."""
+    import torch
+    N, d, Vs = _check_inputs(H, W_shard, y)
+    opts = make_opts(**opt_kw)
+    ws = _chunk_ws(workspace, N, d, Vs, opts, H.device)
+    stats = torch.empty((max(int(rows), 1), 4), dtype=torch.float32, device=H.device)[:int(rows)]
+    rc = load().lce_vshard_chunk_stats(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
+                                       int(c0), int(rows), _ptr(stats), ctypes.byref(opts), _ptr(ws), ws.numel(),
+                                       _stream(stream))
+    _raise(rc, "lce_vshard_chunk_stats")
+    return stats
+
+
+def lce_vshard_chunk_backward(H, W_shard, y, vocab_offset: int, V_total: int, c0: int, rows: int, stats_all, *,
+                              workspace, lse, dH_partial, dW_shard, grad_loss=None, stream=None, **opt_kw):
+    """With the R ranks' statistics of the chunk (stats_all [R, rows, 4], rank
+    order) and the workspace of the stats call: writes lse and dH_partial rows
+    [c0, c0 + rows) and writes (c0 == 0) or adds to dW_shard [V_shard, d]."""
+    import torch
+    N, d, Vs = _check_inputs(H, W_shard, y)
+    opts = make_opts(**opt_kw)
+    ws = _chunk_ws(workspace, N, d, Vs, opts, H.device)
+    _check_grads(H, N, d, Vs, lse=lse, grad_loss=grad_loss, dW=dW_shard)
+    _check_dev(dH_partial, "dH_partial", torch.float32, shape=(N, d), device=H.device)
+    _check_dev(stats_all, "stats_all", torch.float32, device=H.device)
+    if stats_all is None or stats_all.dim() != 3 or stats_all.shape[1:] != (int(rows), 4):
+        raise ValueError(f"stats_all must have shape [R, {int(rows)}, 4]")
+    if lse is None or dH_partial is None or dW_shard is None:
+        raise ValueError("lse, dH_partial and dW_shard are required")
+    rc = load().lce_vshard_chunk_backward(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
+                                          int(c0), int(rows), _ptr(stats_all), int(stats_all.shape[0]),
+                                          _ptr(grad_loss), _ptr(lse), _ptr(dH_partial), _ptr(dW_shard),
+                                          ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
+    _raise(rc, "lce_vshard_chunk_backward")
 
 
 # ---------------------------------------------------------------------------

@@ -75,6 +75,7 @@ extern "C" {
 #define LCE_OP_FWD_BWD 2
 #define LCE_OP_VSHARD_COMBINE 3
 #define LCE_OP_NORM_FWD_BWD 4
+#define LCE_OP_VSHARD_CHUNK 5
 
 /* device status bits returned by lce_read_device_status */
 #define LCE_DEVICE_LABEL_RANGE 1
@@ -221,6 +222,41 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
                         int64_t vocab_offset, int64_t V_total, const float* lse, const float* grad_loss,
                         float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
                         void* stream);
+
+/*
+ * Vocabulary-parallel use without recomputing the logits: 6 N V_shard d flops
+ * per rank instead of the 8 N V_shard d of the three calls above. Per chunk of
+ * rows [c0, c0 + rows) (rows <= the chunk size of opts; c0 = 0 first, chunks
+ * in order):
+ *   1. lce_vshard_chunk_stats -> stats [rows, 4] fp32, the same statistics as
+ *      lce_vshard_forward_stats for those rows; the shard's exp tile
+ *      exp(z - m~) (m~: the row's maximum over the shard's first 128 columns)
+ *      stays in ws for step 3;
+ *   2. the caller all-gathers the R ranks' stats into [R, rows, 4] (rank order);
+ *   3. lce_vshard_chunk_backward with that array and the SAME ws (untouched in
+ *      between) -> lse rows [c0, c0 + rows) of lse [N], dH_partial rows of
+ *      [N, d] fp32 (summed over ranks by the caller: an all-reduce), and
+ *      dW_shard [V_shard, d] fp32, written for c0 == 0 (unless
+ *      opts->accumulate_dW) and added to for later chunks.
+ * The merge in step 3 is lce_vshard_combine's, so the loss of the whole batch
+ * is lce_vshard_combine on the gathered statistics of all chunks [R, N, 4].
+ * The exp tile is exact only within a range: a chunk where it would exceed its
+ * row reference by more than ~e^60 (found in step 1), or where the merged lse
+ * of a row whose label lies in this shard exceeds that row's reference by more
+ * than 60 nats (found in step 3), gets the exact gradient tile recomputed.
+ * Workspace: lce_workspace_size(LCE_OP_VSHARD_CHUNK, N, d, V_shard, opts)
+ * (the chunk's exp tile, its statistics and alpha-scaled rows of H).
+ * Requirements as for the calls above, and 0 <= c0, 0 <= rows, c0 + rows <= N,
+ * 1 <= R <= 4096; stats arrays 16-byte aligned. rows == 0 does nothing.
+ */
+int lce_vshard_chunk_stats(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                           int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t c0, int64_t rows,
+                           float* stats, const lce_opts* opts, void* ws, size_t ws_bytes, void* stream);
+int lce_vshard_chunk_backward(const void* H, const void* W_shard, const int64_t* y, int64_t N, int64_t d,
+                              int64_t V_shard, int64_t vocab_offset, int64_t V_total, int64_t c0, int64_t rows,
+                              const float* stats_all, int64_t R, const float* grad_loss, float* lse,
+                              float* dH_partial, float* dW_shard, const lce_opts* opts, void* ws, size_t ws_bytes,
+                              void* stream);
 
 /*
  * The final zero-centred RMSNorm that produces H ("XTuner on Ascend 910C:

@@ -200,6 +200,44 @@ def test_sliced_bounds_checked_on_host(lib):
         assert call([0, 0, 256, 1000]) in (E.LCE_ERR_CUDA, E.LCE_ERR_UNSUPPORTED_DEVICE)
 
 
+def test_vshard_chunk_calls_checked_on_host(lib):
+    o = lce.make_opts(chunk_tokens=256)
+    P = FAKE
+    N, d, Vs, Vt = 700, 64, 1000, 4000
+
+    def stats(c0=0, rows=256, st=P, off=1000, opts=o):
+        return lib.lce_vshard_chunk_stats(P, P, P, N, d, Vs, off, Vt, c0, rows, st, ctypes.byref(opts), P, 1 << 40,
+                                          None)
+
+    def back(c0=0, rows=256, st=P, R=4, lse=P, dH=P, dW=P):
+        return lib.lce_vshard_chunk_backward(P, P, P, N, d, Vs, 1000, Vt, c0, rows, st, R, None, lse, dH, dW,
+                                             ctypes.byref(o), P, 1 << 40, None)
+
+    E = lce
+    assert stats(rows=257) == E.LCE_ERR_INVALID_ARG          # more rows than the chunk
+    assert stats(c0=600, rows=101) == E.LCE_ERR_INVALID_ARG   # past N
+    assert stats(c0=-1) == E.LCE_ERR_INVALID_ARG
+    assert stats(off=3500) == E.LCE_ERR_INVALID_ARG           # shard past V_total
+    assert stats(st=None) == E.LCE_ERR_INVALID_ARG
+    assert stats(st=P + 8) == E.LCE_ERR_ALIGNMENT
+    assert stats(rows=0, st=None) == E.LCE_OK                 # nothing to do
+    assert back(R=0) == E.LCE_ERR_INVALID_ARG
+    assert back(R=4097) == E.LCE_ERR_INVALID_ARG
+    assert back(dW=None) == E.LCE_ERR_INVALID_ARG
+    assert back(lse=None) == E.LCE_ERR_INVALID_ARG
+    assert back(dH=P + 4) == E.LCE_ERR_ALIGNMENT
+    assert back(st=P + 4) == E.LCE_ERR_ALIGNMENT
+    assert back(rows=0, st=None, lse=None, dH=None) == E.LCE_OK
+    small = lce.workspace_size(lce.LCE_OP_VSHARD_CHUNK, N, d, Vs, o)
+    assert 0 < small < lce.workspace_size(lce.LCE_OP_FWD_BWD, N, d, Vs, o)
+    assert lib.lce_vshard_chunk_stats(P, P, P, N, d, Vs, 1000, Vt, 0, 256, P, ctypes.byref(o), P, small - 1,
+                                      None) == E.LCE_ERR_WORKSPACE
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():      # valid calls get as far as the device check
+        assert stats() in (E.LCE_ERR_CUDA, E.LCE_ERR_UNSUPPORTED_DEVICE)
+        assert back() in (E.LCE_ERR_CUDA, E.LCE_ERR_UNSUPPORTED_DEVICE)
+
+
 def test_slice_bounds_helper():
     b = lce.slice_bounds(151936, 8)
     assert b[0] == 0 and b[-1] == 151936 and len(b) == 9

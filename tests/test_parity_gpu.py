@@ -248,6 +248,73 @@ def test_vocab_shards_on_one_gpu(cuda_lib, cuts, chunk):
     assert ((lse - lse_full).abs() / lse_full.abs()).max().item() <= TOL_LSE
 
 
+def vshard_stored(cuda_lib, H, W, y, cuts, chunk, **kw):
+    """The stored-tile vocabulary-parallel schedule with the shards run in turn
+    on one GPU: per chunk every shard's statistics (each shard keeps its exp
+    tile in its own workspace), their rank-order stack in place of the
+    all-gather, then every shard's chunk backward; the loss from the merge of
+    all chunks' statistics, the partial dH summed by torch in place of the
+    all-reduce. Returns loss, lse, dH (fp32), dW (the shards' rows stacked)."""
+    torch = _torch()
+    N, d = H.shape
+    V = W.shape[0]
+    shards = list(zip(cuts[:-1], cuts[1:]))
+    C = max(1, min(chunk or 4096, N))
+    ws = [cuda_lib.vshard_chunk_workspace(H, W[a:b], y, chunk_tokens=C, **kw) for a, b in shards]
+    lse = torch.empty(N, dtype=torch.float32, device="cuda")
+    dHp = [torch.empty((N, d), dtype=torch.float32, device="cuda") for _ in shards]
+    dW = torch.empty((V, d), dtype=torch.float32, device="cuda")
+    per_chunk = []
+    for c0 in range(0, N, C):
+        rows = min(C, N - c0)
+        st = torch.stack([cuda_lib.lce_vshard_chunk_stats(H, W[a:b], y, a, V, c0, rows, workspace=ws[k],
+                                                          chunk_tokens=C, **kw)
+                          for k, (a, b) in enumerate(shards)]).contiguous()
+        for k, (a, b) in enumerate(shards):
+            cuda_lib.lce_vshard_chunk_backward(H, W[a:b], y, a, V, c0, rows, st, workspace=ws[k], lse=lse,
+                                               dH_partial=dHp[k], dW_shard=dW[a:b], chunk_tokens=C, **kw)
+        per_chunk.append(st)
+    loss, lse2 = cuda_lib.lce_vshard_combine(torch.cat(per_chunk, dim=1).contiguous(), y, V, **kw)
+    assert torch.equal(lse, lse2)          # the chunk backward's merge is the combine's
+    dH = dHp[0]
+    for p in dHp[1:]:
+        dH += p
+    return loss, lse, dH, dW
+
+
+@pytest.mark.parametrize("cuts,chunk", [((0, 1000, 2600, 4099), 0), ((0, 257, 4099), 200), ((0, 4000, 4099), 512)])
+def test_vocab_shards_stored_tiles(cuda_lib, cuts, chunk):
+    """The stored-tile shard calls (statistics and exp tile per chunk, backward
+    from the kept tile) against the oracle and against the recomputing calls."""
+    torch = _torch()
+    inp = small_inputs(700, 264, 4099, seed=37, sigma_w=0.05)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, W, y = to_dev(inp)
+    loss, lse, dH, dW = vshard_stored(cuda_lib, H, W, y, cuts, chunk, sync_check=True)
+    check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), dH.cpu().numpy().astype(np.float64),
+                         dW.cpu().numpy())
+    stats = [cuda_lib.lce_vshard_forward_stats(H, W[a:b], y, a, 4099, chunk_tokens=chunk)
+             for a, b in zip(cuts[:-1], cuts[1:])]
+    loss_r, lse_r = cuda_lib.lce_vshard_combine(torch.stack(stats).contiguous(), y, 4099)
+    assert torch.equal(lse, lse_r) and torch.equal(loss, loss_r)   # the same statistics, merged the same way
+
+
+def test_vocab_shards_stored_tiles_guard(cuda_lib):
+    """A word far above its shard's row reference (outside the shard's first
+    128 words) trips that shard's guard: its chunk gets the exact gradient tile
+    from the exchanged statistics; the other shard keeps its stored tile."""
+    inp = small_inputs(300, 64, 1000, seed=17, sigma_w=0.05)
+    W = inputs.bf16_bits_to_f32(inp["W"]).astype(np.float64)
+    W[700] = 10.0                                  # z_{i,700} = 10 * sum_k H_ik ~ N(0, 80^2)
+    inp["W"] = inputs.f64_to_bf16_bits(W)
+    ref = oracle.lce_bf16(inp["H"], inp["W"], inp["y"])
+    H, Wd, y = to_dev(inp)
+    for chunk in (0, 128):
+        loss, lse, dH, dW = vshard_stored(cuda_lib, H, Wd, y, (0, 500, 1000), chunk, sync_check=True)
+        check_against_oracle(ref, inp["y"], loss.item(), lse.cpu().numpy(), dH.cpu().numpy().astype(np.float64),
+                             dW.cpu().numpy())
+
+
 @pytest.mark.parametrize("N,d", [(300, 64), (517, 2048), (130, 7168)])
 def test_rmsnorm_forward_backward(cuda_lib, N, d):
     torch = _torch()
@@ -482,6 +549,17 @@ def test_full_qwen2b_vocab_shards(cuda_lib):
         return loss, lse, dH, dW
 
     sampled_full_check(cuda_lib, "qwen2b_n8192_d2048_v151936", compute=shards)
+
+
+def test_full_qwen2b_vocab_shards_stored(cuda_lib):
+    """The stored-tile shard calls at the bench workload (bench.py --path
+    vshard): four uneven shards run in turn on one GPU, chunk 4096."""
+
+    def stored(H, W, y):
+        V = W.shape[0]
+        return vshard_stored(cuda_lib, H, W, y, [0, 37000, 76032, 114000, V], 4096)
+
+    sampled_full_check(cuda_lib, "qwen2b_n8192_d2048_v151936", compute=stored)
 
 
 def test_full_qwen2b_norm_fwd_bwd(cuda_lib):
