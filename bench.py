@@ -240,6 +240,9 @@ def main():
                          "--shards shards run in turn on one GPU (partial dH summed by torch in place of the "
                          "all-reduce)")
     ap.add_argument("--shards", type=int, default=4, help="with --path vshard: number of vocabulary shards")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured once into a CUDA graph and replayed (one GPU; reported as "
+                         "'graph' beside the eager value)")
     ap.add_argument("--vshard-method", default="stored", choices=["stored", "recompute"],
                     help="with --path vshard: the per-chunk calls keeping the exp tile (lce_vshard_chunk_*), or the "
                          "three calls that recompute the logits in the backward")
@@ -407,6 +410,30 @@ def main():
            "h2d_bytes_per_step": H_host.numel() * 2 + y_host.numel() * 8, "d2h_bytes_per_step": 4,
            "loss_last_step": float(loss_host.item())}
 
+    # ---- the same step captured into a CUDA graph and replayed (launch cost off the host path)
+    graph = None
+    if args.graph and world == 1:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step(H, y)
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(H, y)
+        for _ in range(3):
+            g.replay()
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+        barrier()
+        ms_g = ev0.elapsed_time(ev1)
+        graph = {"value": N * args.steps / (ms_g * 1e-3), "unit": UNIT, "ms_per_step": ms_g / args.steps,
+                 "how": "one step captured with torch.cuda.graph and replayed; device-resident inputs"}
+        del g
+
     cublas = None
     if args.cublas_logits:
         C = chunk if chunk > 0 else N
@@ -482,6 +509,7 @@ def main():
         "roofline": roof, "kernels": kernels, "gpu_launches": gpu_launches, "e2e": e2e, "clocks": clk,
         **({"hbm_kernels": hbm_kernels} if hbm_kernels else {}),
         **({"cublas_logits_gemm": cublas} if cublas else {}),
+        **({"graph": graph} if graph else {}),
         "extra_device_bytes": int(ws.numel()), "unfused_logits_bytes": N * V * 4,
     }
     if world == 1 and not args.no_cpu_baseline:

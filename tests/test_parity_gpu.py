@@ -433,6 +433,37 @@ def test_label_out_of_range_is_reported_and_ignored(cuda_lib):
     check_against_oracle(ref, y_ign, loss.item(), lse.cpu().numpy(), bf16_to_np(dH), dW.cpu().numpy())
 
 
+def test_cuda_graph_capture_and_replay(cuda_lib):
+    """lce_fwd_bwd captured into a CUDA graph (its launches, tensor maps and
+    workspace carve-up fixed at capture) and replayed on new inputs copied into
+    the captured buffers gives the eager call's results bit for bit."""
+    torch = _torch()
+    N, d, V, chunk = 700, 256, 4096, 256
+    H, W, y = to_dev(small_inputs(N, d, V, seed=71))
+    ws = torch.empty(cuda_lib.workspace_size(cuda_lib.LCE_OP_FWD_BWD, N, d, V, cuda_lib.make_opts(chunk_tokens=chunk)),
+                     dtype=torch.uint8, device="cuda")
+    dW = torch.empty((V, d), dtype=torch.float32, device="cuda")
+    lse = torch.empty(N, dtype=torch.float32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                       # warm-up off the default stream, as torch asks
+        cuda_lib.lce_fwd_bwd(H, W, y, dW=dW, lse=lse, workspace=ws, chunk_tokens=chunk)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        loss, lse_g, dH, dW_g = cuda_lib.lce_fwd_bwd(H, W, y, dW=dW, lse=lse, workspace=ws, chunk_tokens=chunk)
+    for seed in (72, 73):
+        H2, W2, y2 = to_dev(small_inputs(N, d, V, seed=seed))
+        H.copy_(H2)
+        W.copy_(W2)
+        y.copy_(y2)
+        g.replay()
+        ref = cuda_lib.lce_fwd_bwd(H2, W2, y2, chunk_tokens=chunk)
+        torch.cuda.synchronize()
+        for a, b in zip((loss, lse_g, dH, dW_g), ref):
+            assert torch.equal(a, b)
+
+
 def test_chunk_size_invariance_and_determinism(cuda_lib):
     """loss, lse and dH are row-local with a fixed vocabulary order: bitwise
     equal for every chunk size; dW differs only by fp32 reassociation."""
