@@ -252,6 +252,12 @@ def _workspace(op, N, d, V, opts, device, workspace=None):
     return torch.empty(need, dtype=torch.uint8, device=device)
 
 
+def _no_accumulate_without_dW(opts):
+    """accumulate_dW adds into the caller's dW: without one there is nothing to add to."""
+    if opts.accumulate_dW:
+        raise ValueError("accumulate_dW=True needs the dW tensor to accumulate into")
+
+
 def _raise(rc, where):
     if rc != LCE_OK:
         raise LCEError(rc, where)
@@ -287,6 +293,7 @@ def lce_backward(H, W, y, lse, grad_loss=None, *, dW=None, workspace=None, strea
     ws = _workspace(LCE_OP_BACKWARD, N, d, V, opts, H.device, workspace)
     dH = torch.empty_like(H)
     if dW is None:
+        _no_accumulate_without_dW(opts)
         dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
     rc = load().lce_backward(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW),
                              ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
@@ -308,6 +315,7 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
         lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
     dH = torch.empty_like(H)
     if dW is None:
+        _no_accumulate_without_dW(opts)
         dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
     rc = load().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(dH),
                             _ptr(dW), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
@@ -374,6 +382,7 @@ def lce_fwd_bwd_sliced(H, W, y, grad_loss=None, *, bounds, events=None, sm_limit
         lse = torch.empty(max(N, 1), dtype=torch.float32, device=H.device)[:N]
     dH = torch.empty_like(H)
     if dW is None:
+        _no_accumulate_without_dW(opts)
         dW = torch.empty((V, d), dtype=torch.float32, device=H.device)
     b = (ctypes.c_int64 * (n + 1))(*[int(x) for x in bounds])
     ev = None
@@ -509,6 +518,7 @@ def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, gra
     ws = _workspace(LCE_OP_BACKWARD, N, d, Vs, opts, H.device, workspace)
     dH = torch.empty((N, d), dtype=torch.float32, device=H.device)
     if dW is None:
+        _no_accumulate_without_dW(opts)
         dW = torch.empty((Vs, d), dtype=torch.float32, device=H.device)
     rc = load().lce_vshard_backward(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
                                     _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW), ctypes.byref(opts), _ptr(ws),
@@ -630,6 +640,7 @@ def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, work
     dx = torch.empty_like(x)
     dw_norm = torch.empty(d, dtype=torch.float32, device=x.device)
     if dW is None:
+        _no_accumulate_without_dW(opts)
         dW = torch.empty((V, d), dtype=torch.float32, device=x.device)
     rc = load().lce_norm_fwd_bwd(_ptr(x), _ptr(w_norm), float(eps), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss),
                                  _ptr(loss), _ptr(lse), _ptr(dx), _ptr(dw_norm), _ptr(dW), ctypes.byref(opts),

@@ -63,6 +63,8 @@ def vocab_parallel_fwd_bwd(H, W_shard, y, vocab_offset: int, V_total: int, grad_
         dist.all_reduce(dH, group=group)
         return loss, lse, dH, dW_shard
 
+    if opt_kw.get("accumulate_dW"):
+        raise ValueError("the stored schedule returns a new dW_shard; add it to an accumulator yourself")
     N, d = H.shape
     Vs = W_shard.shape[0]
     ftype = torch.float64 if H.dtype == torch.float64 else torch.float32

@@ -392,6 +392,11 @@ def test_binding_rejects_bad_caller_tensors(cuda_lib):
         cuda_lib.lce_backward(H, W, y, torch.zeros(64, dtype=torch.float16, device="cuda"))
     with pytest.raises(ValueError):
         cuda_lib.lce_scale_grads(None, torch.zeros(300, 64, device="cuda"), torch.ones(1, device="cuda").half())
+    # accumulating needs the caller's dW to add into
+    with pytest.raises(ValueError):
+        cuda_lib.lce_fwd_bwd(H, W, y, accumulate_dW=True)
+    with pytest.raises(ValueError):
+        cuda_lib.lce_backward(H, W, y, torch.zeros(64, device="cuda"), accumulate_dW=True)
 
 
 def test_all_ignored_and_empty(cuda_lib):
