@@ -258,6 +258,18 @@ def _no_accumulate_without_dW(opts):
         raise ValueError("accumulate_dW=True needs the dW tensor to accumulate into")
 
 
+def _keep(stream, *tensors):
+    """Tensors a call used on a stream other than the current one: tell the
+    caching allocator, so that their memory is not handed out again while that
+    stream's kernels may still use it (the workspace is freed as the wrapper
+    returns)."""
+    if stream is None:
+        return
+    for t in tensors:
+        if t is not None:
+            t.record_stream(stream)
+
+
 def _raise(rc, where):
     if rc != LCE_OK:
         raise LCEError(rc, where)
@@ -276,6 +288,7 @@ def lce_forward(H, W, y, *, workspace=None, stream=None, **opt_kw):
     rc = load().lce_forward(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(loss), _ptr(lse), ctypes.byref(opts),
                             _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_forward")
+    _keep(stream, ws, loss, lse)
     return loss, lse
 
 
@@ -298,6 +311,7 @@ def lce_backward(H, W, y, lse, grad_loss=None, *, dW=None, workspace=None, strea
     rc = load().lce_backward(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW),
                              ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_backward")
+    _keep(stream, ws, dH, dW, lse, grad_loss)
     return dH, dW
 
 
@@ -320,6 +334,7 @@ def lce_fwd_bwd(H, W, y, grad_loss=None, *, dW=None, lse=None, workspace=None, s
     rc = load().lce_fwd_bwd(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(grad_loss), _ptr(loss), _ptr(lse), _ptr(dH),
                             _ptr(dW), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_fwd_bwd")
+    _keep(stream, ws, loss, lse, dH, dW, grad_loss)
     return loss, lse, dH, dW
 
 
@@ -343,6 +358,7 @@ def lce_forward_noalloc(H, W, y, *, loss=None, lse=None, stream=None, **opt_kw):
     rc = load().lce_forward_noalloc(_ptr(H), _ptr(W), _ptr(y), N, d, V, _ptr(loss), _ptr(lse), ctypes.byref(opts),
                                     _stream(stream))
     _raise(rc, "lce_forward_noalloc")
+    _keep(stream, loss, lse)
     return loss, lse
 
 
@@ -397,6 +413,7 @@ def lce_fwd_bwd_sliced(H, W, y, grad_loss=None, *, bounds, events=None, sm_limit
                                    _ptr(dH), _ptr(dW), n, b, ev, int(sm_limit), ctypes.byref(opts), _ptr(ws),
                                    ws.numel(), _stream(stream))
     _raise(rc, "lce_fwd_bwd_sliced")
+    _keep(stream, ws, loss, lse, dH, dW, grad_loss)
     return loss, lse, dH, dW
 
 
@@ -481,6 +498,7 @@ def lce_vshard_forward_stats(H, W_shard, y, vocab_offset: int, V_total: int, *, 
     rc = load().lce_vshard_forward_stats(_ptr(H), _ptr(W_shard), _ptr(y), N, d, Vs, int(vocab_offset), int(V_total),
                                          _ptr(stats), ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_forward_stats")
+    _keep(stream, ws, stats)
     return stats
 
 
@@ -503,6 +521,7 @@ def lce_vshard_combine(stats_all, y, V_total: int, *, workspace=None, stream=Non
     rc = load().lce_vshard_combine(_ptr(stats_all), R, _ptr(y), N, int(V_total), _ptr(lse), _ptr(loss),
                                    ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_combine")
+    _keep(stream, ws, loss, lse)
     return loss, lse
 
 
@@ -524,6 +543,7 @@ def lce_vshard_backward(H, W_shard, y, vocab_offset: int, V_total: int, lse, gra
                                     _ptr(lse), _ptr(grad_loss), _ptr(dH), _ptr(dW), ctypes.byref(opts), _ptr(ws),
                                     ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_backward")
+    _keep(stream, ws, dH, dW, lse, grad_loss)
     return dH, dW
 
 
@@ -554,6 +574,7 @@ def lce_vshard_chunk_stats(H, W_shard, y, vocab_offset: int, V_total: int, c0: i
                                        int(c0), int(rows), _ptr(stats), ctypes.byref(opts), _ptr(ws), ws.numel(),
                                        _stream(stream))
     _raise(rc, "lce_vshard_chunk_stats")
+    _keep(stream, ws, stats)
     return stats
 
 
@@ -578,6 +599,7 @@ def lce_vshard_chunk_backward(H, W_shard, y, vocab_offset: int, V_total: int, c0
                                           _ptr(grad_loss), _ptr(lse), _ptr(dH_partial), _ptr(dW_shard),
                                           ctypes.byref(opts), _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_vshard_chunk_backward")
+    _keep(stream, ws, stats_all, lse, dH_partial, dW_shard, grad_loss)
 
 
 # ---------------------------------------------------------------------------
@@ -602,6 +624,7 @@ def lce_rmsnorm_forward(x, w, eps=1e-6, *, stream=None):
     rstd = torch.empty(max(N, 1), dtype=torch.float32, device=x.device)[:N]
     _raise(load().lce_rmsnorm_forward(_ptr(x), _ptr(w), N, d, float(eps), _ptr(H), _ptr(rstd), _stream(stream)),
            "lce_rmsnorm_forward")
+    _keep(stream, H, rstd)
     return H, rstd
 
 
@@ -619,6 +642,7 @@ def lce_rmsnorm_backward(x, w, rstd, dH, *, stream=None):
     ws = torch.empty(need, dtype=torch.uint8, device=x.device)
     _raise(load().lce_rmsnorm_backward(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dH), N, d, _ptr(dx), _ptr(dw), _ptr(ws),
                                        ws.numel(), _stream(stream)), "lce_rmsnorm_backward")
+    _keep(stream, ws, dx, dw)
     return dx, dw
 
 
@@ -646,6 +670,7 @@ def lce_norm_fwd_bwd(x, w_norm, W, y, grad_loss=None, eps=1e-6, *, dW=None, work
                                  _ptr(loss), _ptr(lse), _ptr(dx), _ptr(dw_norm), _ptr(dW), ctypes.byref(opts),
                                  _ptr(ws), ws.numel(), _stream(stream))
     _raise(rc, "lce_norm_fwd_bwd")
+    _keep(stream, ws, loss, lse, dx, dw_norm, dW, grad_loss)
     return loss, lse, dx, dw_norm, dW
 
 

@@ -469,6 +469,27 @@ def test_cuda_graph_capture_and_replay(cuda_lib):
             assert torch.equal(a, b)
 
 
+def test_two_streams_at_once(cuda_lib):
+    """Calls on two streams with their own workspaces, issued interleaved so that
+    their kernels may run side by side: each gives what it gives alone."""
+    torch = _torch()
+    probs = [to_dev(small_inputs(700, 256, 4096, seed=s)) for s in (91, 92)]
+    alone = [cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256) for H, W, y in probs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    outs = [[], []]
+    for _ in range(3):
+        for k, (H, W, y) in enumerate(probs):
+            outs[k].append(cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256, stream=streams[k]))
+    torch.cuda.synchronize()
+    for k in range(2):
+        for o in outs[k]:
+            for a, b in zip(o, alone[k]):
+                assert torch.equal(a, b)
+
+
 def test_chunk_size_invariance_and_determinism(cuda_lib):
     """loss, lse and dH are row-local with a fixed vocabulary order: bitwise
     equal for every chunk size; dW differs only by fp32 reassociation."""
