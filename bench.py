@@ -280,7 +280,7 @@ def main():
     W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
     H = H_host.to(dev)
     y = y_host.to(dev)
-    n_global = dp.global_valid_count(y) if world > 1 else -1
+    n_global = dp.global_valid_count(y, V=V) if world > 1 else -1
 
     chunk = min(args.chunk, N) if args.chunk > 0 else 0
     opts = dict(chunk_tokens=chunk, n_valid_override=n_global)

@@ -13,11 +13,15 @@ losses and dW equals the unsharded result.
 from __future__ import annotations
 
 
-def global_valid_count(y, ignore_index: int = -100, group=None) -> int:
-    """All-reduce (sum) of the number of labels != ignore_index."""
+def global_valid_count(y, ignore_index: int = -100, group=None, *, V: int) -> int:
+    """All-reduce (sum) of the number of labels the library counts: those that
+    are not ignore_index and lie in [0, V). A label outside the vocabulary is
+    an error the library reports (a device status bit) while it treats that
+    row as ignored, so counting it here would give the ranks a denominator the
+    one-rank call does not use."""
     import torch
     import torch.distributed as dist
-    n = (y != ignore_index).sum().to(torch.int64).reshape(1)
+    n = ((y != ignore_index) & (y >= 0) & (y < V)).sum().to(torch.int64).reshape(1)
     dist.all_reduce(n, group=group)
     return int(n.item())
 
@@ -35,7 +39,7 @@ def dp_fwd_bwd(H, W, y, grad_loss=None, *, n_global: int | None = None, group=No
         from . import lce
         compute = lce.lce_fwd_bwd
     if n_global is None:
-        n_global = global_valid_count(y, ignore_index, group)
+        n_global = global_valid_count(y, ignore_index, group, V=W.shape[0])
     loss, lse, dH, dW = compute(H, W, y, grad_loss, n_valid_override=n_global, ignore_index=ignore_index,
                                 **opt_kw)
     dist.all_reduce(dW, group=group)

@@ -101,7 +101,7 @@ def fsdp_fwd_bwd(H, W, y, grad_loss=None, *, owners: list, slices: list | None =
     if len(owners) != world + 1 or owners[0] != 0 or owners[-1] != W.shape[0]:
         raise ValueError("owners must hold world + 1 bounds from 0 to V")
     slices = owners if slices is None else slices
-    n_global = dp.global_valid_count(y, ignore_index, group)
+    n_global = dp.global_valid_count(y, ignore_index, group, V=W.shape[0])
     cuda = backend is None
     if cuda:
         from . import lce

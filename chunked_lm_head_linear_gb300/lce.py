@@ -240,13 +240,18 @@ def _check_dev(t, name, dtype, numel=None, shape=None, device=None):
 
 
 def _workspace(op, N, d, V, opts, device, workspace=None):
+    """The caller's workspace if it is large enough (else LCE_ERR_WORKSPACE, as
+    the C ABI answers: a caller that sized its own workspace, to bound memory or
+    for graph capture, must not get a hidden allocation); a new one only when
+    the caller passed none."""
     import torch
     need = workspace_size(op, N, d, V, opts)
     if need == 0:
         raise LCEError(LCE_ERR_INVALID_ARG, "lce_workspace_size")
     if workspace is not None:
         _check_dev(workspace, "workspace", torch.uint8, device=device)
-    if workspace is not None and workspace.numel() >= need:
+        if workspace.numel() < need:
+            raise LCEError(LCE_ERR_WORKSPACE, f"workspace of {workspace.numel()} bytes, the call needs {need}")
         return workspace
     # torch's allocator returns 512-byte aligned blocks
     return torch.empty(need, dtype=torch.uint8, device=device)
@@ -511,11 +516,7 @@ def lce_vshard_combine(stats_all, y, V_total: int, *, workspace=None, stream=Non
     _check_dev(stats_all, "stats_all", torch.float32)
     _check_dev(y, "y", torch.int64, shape=(N,), device=stats_all.device)
     opts = make_opts(**opt_kw)
-    need = workspace_size(LCE_OP_VSHARD_COMBINE, N, 8, V_total, opts)
-    if workspace is not None:
-        _check_dev(workspace, "workspace", torch.uint8, device=stats_all.device)
-    ws = workspace if workspace is not None and workspace.numel() >= need else \
-        torch.empty(need, dtype=torch.uint8, device=stats_all.device)
+    ws = _workspace(LCE_OP_VSHARD_COMBINE, N, 8, V_total, opts, stats_all.device, workspace)
     lse = torch.empty(max(N, 1), dtype=torch.float32, device=stats_all.device)[:N]
     loss = torch.empty(1, dtype=torch.float32, device=stats_all.device)
     rc = load().lce_vshard_combine(_ptr(stats_all), R, _ptr(y), N, int(V_total), _ptr(lse), _ptr(loss),

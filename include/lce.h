@@ -182,9 +182,13 @@ int lce_fwd_bwd_sliced(const void* H, const void* W, const int64_t* y, int64_t N
  * is a fixed 32 MiB array inside the library's device image, held on every
  * GPU that loads the library until the process exits; a call whose forward
  * workspace (lce_workspace_size(LCE_OP_FORWARD, ...)) exceeds 32 MiB returns
- * LCE_ERR_WORKSPACE (pass a smaller opts->chunk_tokens). The first call on a
- * device looks up the array's device address (make it before any stream
- * capture). All calls share the one array: calls whose work overlaps on the
+ * LCE_ERR_WORKSPACE (pass a smaller opts->chunk_tokens). The array's device
+ * address belongs to one CUDA context (the device's primary context, a
+ * context the caller created with the driver API, or the new primary context
+ * after cudaDeviceReset each hold their own copy of the library's device
+ * image): the first call in each context looks it up, with that context
+ * current, and caches it under the context's id, so make the first call in a
+ * context before any stream capture in it. All calls share the one array: calls whose work overlaps on the
  * GPU (other streams, other host threads) race and must be serialised by the
  * caller. Nothing in the array needs to be zero on entry; each call
  * overwrites what it reads, and lce_read_device_status() does not apply. */

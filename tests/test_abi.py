@@ -257,3 +257,20 @@ def test_binding_validates_caller_tensors():
     torch = pytest.importorskip("torch")
     with pytest.raises(ValueError, match="CUDA tensor"):
         lce._check_dev(torch.zeros(4, 8), "dW", torch.float32)
+
+
+def test_binding_refuses_undersized_caller_workspace(lib, monkeypatch):
+    """A workspace the caller passes is used as it is or refused with
+    LCE_ERR_WORKSPACE (the C ABI's answer), never silently replaced by a larger
+    hidden allocation; only a call without one gets a new workspace."""
+    torch = pytest.importorskip("torch")
+    monkeypatch.setattr(lce, "_check_dev", lambda *a, **k: None)   # CPU tensors stand in for device ones
+    need = lce.workspace_size(lce.LCE_OP_FWD_BWD, 700, 64, 1000)
+    small = torch.zeros(need - 1, dtype=torch.uint8)
+    with pytest.raises(lce.LCEError) as err:
+        lce._workspace(lce.LCE_OP_FWD_BWD, 700, 64, 1000, None, torch.device("cpu"), small)
+    assert err.value.code == lce.LCE_ERR_WORKSPACE
+    exact = torch.zeros(need, dtype=torch.uint8)
+    assert lce._workspace(lce.LCE_OP_FWD_BWD, 700, 64, 1000, None, torch.device("cpu"), exact) is exact
+    fresh = lce._workspace(lce.LCE_OP_FWD_BWD, 700, 64, 1000, None, torch.device("cpu"), None)
+    assert fresh.numel() == need

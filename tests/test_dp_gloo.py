@@ -71,3 +71,27 @@ def test_two_gloo_ranks_equal_unsharded(tmp_path):
         np.testing.assert_allclose(r["dW"], whole["dW"], rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(np.concatenate([r0["dH"], r1["dH"]]), whole["dH"], rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(np.concatenate([r0["lse"], r1["lse"]]), whole["lse"], rtol=1e-14)
+
+
+def _count_rank(rank, world, port, outdir):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from chunked_lm_head_linear_gb300 import dp
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    y = torch.tensor([[5, -100, 31, -1, 0, 30], [7, 10 ** 9, -100, -100, 2, 3]][rank])
+    n = dp.global_valid_count(y, V=31)
+    np.save(os.path.join(outdir, f"count{rank}.npy"), np.array([n]))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_global_count_follows_the_library_rule(tmp_path):
+    """The data-parallel denominator counts a label only if it is not
+    ignore_index and lies in [0, V), as the library's own label scan does:
+    31, -1 and 10**9 are out of range for V = 31 and are not counted."""
+    port = _free_port()
+    mp.start_processes(_count_rank, args=(2, port, str(tmp_path)), nprocs=2, join=True, start_method="spawn")
+    for r in range(2):
+        assert int(np.load(tmp_path / f"count{r}.npy")[0]) == 3 + 3   # {5, 0, 30} and {7, 2, 3}

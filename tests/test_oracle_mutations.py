@@ -25,8 +25,20 @@ MUTATIONS = {
 }
 
 
+# Plausible mistakes in the fp64 -> bf16 rounding of the norm output, caught by
+# the rounding pin (PyTorch's cast and hand-checked ties).
+ROUNDING_MUTATIONS = {
+    "bf16_truncation": ("return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)",
+                        "return (u >> 16).astype(np.uint16)"),
+    "bf16_ties_away_from_zero": ("return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)",
+                                 "return ((u + 0x8000) >> 16).astype(np.uint16)"),
+    "bf16_ties_to_odd": ("return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)",
+                         "return ((u + 0x8000 - ((u >> 16) & 1)) >> 16).astype(np.uint16)"),
+}
+
+
 def _mutant(name):
-    old, new = MUTATIONS[name]
+    old, new = {**MUTATIONS, **ROUNDING_MUTATIONS}[name]
     src = open(SRC).read()
     assert src.count(old) >= 1, f"mutation anchor for {name} not found"
     mod = types.ModuleType("mutant_" + name)
@@ -81,3 +93,10 @@ def test_unmutated_oracle_passes_the_pins():
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pins_catch_planted_mistake(name):
     assert not _pins_pass(_mutant(name)), f"pins did not catch mutation {name}"
+
+
+@pytest.mark.parametrize("name", sorted(ROUNDING_MUTATIONS))
+def test_rounding_pin_catches_planted_mistake(name):
+    from test_oracle_pins import bf16_rounding_pin_holds
+    assert bf16_rounding_pin_holds(oracle.round_bf16_bits)
+    assert not bf16_rounding_pin_holds(_mutant(name).round_bf16_bits), f"rounding pin did not catch {name}"

@@ -455,3 +455,44 @@ def test_norm_then_cross_entropy_chain_rule():
     assert out["loss"] == pytest.approx(L.item(), rel=1e-12)
     assert _rel(out["dx"], xt.grad.numpy()) < 1e-11
     assert _rel(out["dw_norm"], wt.grad.numpy()) < 1e-11
+
+
+def _bf16_pin_vector():
+    """Finite fp64 values that exercise every branch of fp32 -> bf16 rounding:
+    random magnitudes over 24 decades, exact ties in both directions (1 + 2^-8
+    rounds down to 1, 1 + 3 * 2^-8 rounds up to 1 + 2^-6), near-ties just above and below
+    a tie, signed zeros, subnormals, the largest fp32 values (which round up to
+    infinity in bf16) and negative copies of all of them."""
+    rng = np.random.default_rng(0)
+    base = rng.standard_normal(20000) * 10 ** rng.uniform(-12, 12, 20000)
+    ties = np.array([1.00390625, 1.01171875, 1.005859375, 1.0 + 2 ** -8 + 2 ** -20, 1.0 + 2 ** -8 - 2 ** -20,
+                     2.0 ** -126 * 1.00390625, 2.0 ** -140, 2.0 ** -149, 3.0e-39, 0.0, -0.0,
+                     3.3895313892515355e38, 3.4e38, 3.4028234663852886e38, 65504.0, 1.0, 0.5])
+    x = np.concatenate([base, ties])
+    return np.concatenate([x, -x])
+
+
+def bf16_rounding_pin_holds(round_fn) -> bool:
+    """True if ``round_fn`` (fp64 values -> bf16 bit patterns) agrees with
+    PyTorch's float32 -> bfloat16 cast on the pin vector and on the exact values
+    whose answer is known without any library."""
+    torch = pytest.importorskip("torch")
+    x = _bf16_pin_vector()
+    ours = np.asarray(round_fn(x))
+    ref = torch.tensor(x).to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if not np.array_equal(ours, ref):
+        return False
+    known = {1.00390625: 0x3F80,             # tie: the even neighbour below
+             1.01171875: 0x3F82,             # tie: the even neighbour above
+             1.005859375: 0x3F81,            # three quarters of an ulp: up
+             -1.00390625: 0xBF80,
+             3.4028234663852886e38: 0x7F80}  # past the largest bf16: infinity
+    return all(int(round_fn([v])[0]) == b for v, b in known.items())
+
+
+def test_round_bf16_bits_matches_torch_cast():
+    """The oracle's fp64 -> fp32 -> bf16 rounding of the norm output ("XTuner on
+    Ascend 910C", section 3.1.1: one bf16 rounding of x r (1 + w)) is
+    round-to-nearest-even, pinned against PyTorch's own float32 -> bfloat16
+    cast on values it could plausibly get wrong (ties, overflow, subnormals)."""
+    assert bf16_rounding_pin_holds(oracle.round_bf16_bits)

@@ -40,13 +40,40 @@ def test_dp_one_rank_equals_fused_call(cuda_lib, one_rank_nccl):
     from chunked_lm_head_linear_gb300 import dp
     inp = small_inputs(700, 256, 4096, seed=81)
     H, W, y = to_dev(inp)
-    n = dp.global_valid_count(y)
+    n = dp.global_valid_count(y, V=4096)
     assert n == int((inp["y"] != oracle.IGNORE_INDEX).sum())
     loss, lse, dH, dW = dp.dp_fwd_bwd(H, W, y, n_global=n, chunk_tokens=256)
     ref = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256)
     torch.cuda.synchronize()
     for a, b in zip((loss, lse, dH, dW), ref):
         assert torch.equal(a, b)
+
+
+def test_dp_count_with_out_of_range_labels_matches_the_library(cuda_lib, one_rank_nccl):
+    """Labels outside the vocabulary (an error the library reports and whose
+    rows it treats as ignored) are not counted in the data-parallel
+    denominator either: the DP step equals the one-rank call bit for bit, and
+    the count equals the one the library itself took."""
+    import torch
+    from chunked_lm_head_linear_gb300 import dp
+    inp = small_inputs(700, 256, 4096, seed=82)
+    inp["y"][[3, 100, 555]] = [4096, -7, 10 ** 9]
+    H, W, y = to_dev(inp)
+    n = dp.global_valid_count(y, V=4096)
+    valid = (inp["y"] != oracle.IGNORE_INDEX) & (inp["y"] >= 0) & (inp["y"] < 4096)
+    assert n == int(valid.sum())
+    ws = torch.empty(cuda_lib.workspace_size(cuda_lib.LCE_OP_FWD_BWD, 700, 256, 4096,
+                                             cuda_lib.make_opts(chunk_tokens=256)), dtype=torch.uint8, device="cuda")
+    loss, lse, dH, dW = dp.dp_fwd_bwd(H, W, y, n_global=n, chunk_tokens=256)
+    ref = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256, workspace=ws)
+    flags = cuda_lib.read_device_status(ws)
+    assert flags & cuda_lib.LCE_DEVICE_LABEL_RANGE
+    # equal mean losses and gradients bit for bit: the two denominators agree
+    for a, b in zip((loss, lse, dH, dW), ref):
+        assert torch.equal(a, b)
+    # the shards' own counts add up to the same denominator
+    halves = [dp.global_valid_count(y[:350], V=4096), dp.global_valid_count(y[350:], V=4096)]
+    assert sum(halves) == n
 
 
 @pytest.mark.parametrize("method,chunk", [("stored", 256), ("stored", 0), ("recompute", 0)])

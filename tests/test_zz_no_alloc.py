@@ -82,3 +82,100 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
                                  ctypes.c_void_p(y.data_ptr()), 8192, 64, 151936, ctypes.c_void_p(H.data_ptr()),
                                  ctypes.c_void_p(H.data_ptr()), ctypes.byref(opts), None)
     assert rc == cuda_lib.LCE_ERR_WORKSPACE
+
+
+_CONTEXT_SCRIPT = r'''
+import ctypes, sys
+import numpy as np
+sys.path.insert(0, sys.argv[1])
+from chunked_lm_head_linear_gb300 import inputs, lce
+
+cu = ctypes.CDLL("libcuda.so.1")
+
+
+def ck(rc, what):
+    if rc != 0:
+        raise SystemExit(f"{what} returned {rc}")
+
+
+def dalloc(n):
+    p = ctypes.c_uint64()
+    ck(cu.cuMemAlloc_v2(ctypes.byref(p), ctypes.c_size_t(max(n, 1))), "cuMemAlloc")
+    return p.value
+
+
+def h2d(a):
+    p = dalloc(a.nbytes)
+    ck(cu.cuMemcpyHtoD_v2(ctypes.c_uint64(p), a.ctypes.data_as(ctypes.c_void_p), ctypes.c_size_t(a.nbytes)), "HtoD")
+    return p
+
+
+def d2h(p, n, dtype):
+    out = np.empty(n, dtype=dtype)
+    ck(cu.cuMemcpyDtoH_v2(out.ctypes.data_as(ctypes.c_void_p), ctypes.c_uint64(p), ctypes.c_size_t(out.nbytes)), "DtoH")
+    return out
+
+
+def run_both(seed):
+    """lce_forward with a workspace and lce_forward_noalloc, in the current context."""
+    lib = lce.load()
+    w = inputs.Workload(f"ctx{seed}", N=700, d=256, V=4096, sigma_w=0.05, labels="uniform", ignore="random",
+                        ignore_frac=0.1, seed=seed)
+    inp = inputs.make_inputs(w)
+    N, d, V = 700, 256, 4096
+    bufs = [h2d(np.ascontiguousarray(inp["H"])), h2d(np.ascontiguousarray(inp["W"])),
+            h2d(np.ascontiguousarray(inp["y"]))]
+    H, W, y = bufs
+    opts = lce.make_opts(chunk_tokens=256, sync_check=True)
+    need = lce.workspace_size(lce.LCE_OP_FORWARD, N, d, V, opts)
+    ws, la, sa, lb, sb = dalloc(need), dalloc(4), dalloc(4 * N), dalloc(4), dalloc(4 * N)
+    bufs += [ws, la, sa, lb, sb]
+    rc = lib.lce_forward(H, W, y, N, d, V, la, sa, ctypes.byref(opts), ws, need, None)
+    ck(rc, "lce_forward")
+    rc = lib.lce_forward_noalloc(H, W, y, N, d, V, lb, sb, ctypes.byref(opts), None)
+    ck(rc, "lce_forward_noalloc")
+    ck(cu.cuCtxSynchronize(), "cuCtxSynchronize")
+    loss_a, loss_b = d2h(la, 1, np.float32)[0], d2h(lb, 1, np.float32)[0]
+    lse_a, lse_b = d2h(sa, N, np.float32), d2h(sb, N, np.float32)
+    for p in bufs:
+        ck(cu.cuMemFree_v2(ctypes.c_uint64(p)), "cuMemFree")
+    assert abs(loss_b - loss_a) <= float(sys.argv[2]) * abs(loss_a), (loss_a, loss_b)
+    rel = np.max(np.abs(lse_b - lse_a) / np.maximum(np.abs(lse_a), 1.0))
+    assert rel <= float(sys.argv[3]), rel
+
+
+ck(cu.cuInit(0), "cuInit")
+dev = ctypes.c_int()
+ck(cu.cuDeviceGet(ctypes.byref(dev), 0), "cuDeviceGet")
+for seed in (11, 12):     # a context of its own, destroyed, then a new one: the library image moves
+    ctx = ctypes.c_void_p()
+    ck(cu.cuCtxCreate_v2(ctypes.byref(ctx), 0, dev), "cuCtxCreate")
+    run_both(seed)
+    ck(cu.cuCtxDestroy_v2(ctx), "cuCtxDestroy")
+prim = ctypes.c_void_p()  # and the device's primary context after them
+ck(cu.cuDevicePrimaryCtxRetain(ctypes.byref(prim), dev), "cuDevicePrimaryCtxRetain")
+ck(cu.cuCtxSetCurrent(prim), "cuCtxSetCurrent")
+run_both(13)
+ck(cu.cuDevicePrimaryCtxRelease_v2(dev), "cuDevicePrimaryCtxRelease")
+print("CONTEXTS_OK")
+'''
+
+
+def test_noalloc_in_contexts_the_caller_creates(cuda_lib, tmp_path):
+    """A caller may run the library in a context it created with the driver
+    API, destroy it and create another: each context holds its own copy of the
+    library's device image, so the scratch array sits at a different device
+    address in each, and lce_forward_noalloc must find the one of the current
+    context (an address from a destroyed or a different context would be
+    wrong memory). Runs in a child process without PyTorch, whose only
+    contexts are the ones made here; each context's result is checked against
+    lce_forward with a workspace in the same context."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    script = tmp_path / "contexts.py"
+    script.write_text(_CONTEXT_SCRIPT)
+    out = subprocess.run([sys.executable, str(script), root, str(TOL_LOSS), str(TOL_LSE)], capture_output=True,
+                         text=True, timeout=300)
+    assert out.returncode == 0 and "CONTEXTS_OK" in out.stdout, out.stdout[-2000:] + out.stderr[-2000:]
