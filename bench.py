@@ -60,7 +60,7 @@ def load_peaks():
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 class ClockSampler:
-    FIELDS = ("uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,uuid,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -69,11 +69,17 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.window = None   # (start, end) host time of the timed region
+
+    def mark(self, start: float, end: float):
+        """The timed region, in host seconds since the epoch: only samples taken
+        inside it count."""
+        self.window = (start, end)
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
-                                          "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                          "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                                          text=True)
         except OSError:
             self.proc = None
@@ -95,27 +101,37 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
+        import datetime
         sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        outside = 0
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 10:
+            if len(parts) < 11:
                 continue
-            if self.uuid and self.uuid not in parts[0]:
+            if self.uuid and self.uuid not in parts[1]:
                 continue
+            if self.window is not None:
+                try:
+                    t = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                except ValueError:
+                    t = None
+                if t is not None and not (self.window[0] <= t <= self.window[1]):
+                    outside += 1
+                    continue
             try:
-                sm.append(float(parts[2].split()[0]))
-                smax.append(float(parts[3].split()[0]))
-                power.append(float(parts[4].split()[0]))
+                sm.append(float(parts[3].split()[0]))
+                smax.append(float(parts[4].split()[0]))
+                power.append(float(parts[5].split()[0]))
             except (ValueError, IndexError):
                 continue
-            for nm, v in zip(names, parts[6:10]):
+            for nm, v in zip(names, parts[7:11]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
                 "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "samples_outside_timed_region": outside, "reasons": sorted(reasons)}
 
 
 def gpu_uuid(torch):
@@ -151,11 +167,15 @@ def cpu_model() -> str:
 
 
 def _rows_for(run, target_s, min_rows, max_rows, step=1):
-    """One warm-up run of ``run(rows) -> seconds`` on ``min_rows`` rows (it
-    also pays one-time costs) gives the time per row; return the number of
-    rows that takes about ``target_s``."""
-    per_row = max(run(min_rows) / min_rows, 1e-6)
-    rows = int(min(max_rows, max(min_rows, target_s / per_row)))
+    """Number of rows for which ``run(rows) -> seconds`` takes about
+    ``target_s``: a warm-up run (one-time costs), then two runs of min_rows
+    and 2 min_rows rows separate the fixed part of a call (e.g. writing the
+    fp64 dW [V, d]) from the part per row."""
+    run(min_rows)
+    t1, t2 = run(min_rows), run(2 * min_rows)
+    per_row = max((t2 - t1) / min_rows, 1e-6)
+    fixed = max(t1 - min_rows * per_row, 0.0)
+    rows = int(min(max_rows, max(min_rows, (target_s - fixed) / per_row)))
     return max(min_rows, rows // step * step)
 
 
@@ -219,7 +239,7 @@ def cpu_baseline(inp, base_name, target_s=5.0):
     w = inp["workload"]
     cores = os.cpu_count() or 1
     Wd = oracle.decode_bf16(inp["W"])
-    rows = _rows_for(lambda r: _time_numpy(inp, r, Wd), target_s, 32, min(4096, w.N), step=32)
+    rows = _rows_for(lambda r: _time_numpy(inp, r, Wd), 2 * target_s, 32, min(4096, w.N), step=32)
     t = _time_numpy(inp, rows, Wd)
     res = {"value": rows / t, "unit": UNIT, "cores": cores, "kind": "oracle", "cpu_model": cpu_model(),
            "sample": f"first {rows} tokens of the workload at full d and V, numpy fp64 oracle "
@@ -230,9 +250,10 @@ def cpu_baseline(inp, base_name, target_s=5.0):
         samples["numpy_one_core"] = {"tokens_per_s": one["rows"] / one["s"], "rows": one["rows"], "s": one["s"],
                                      "threads": 1}
     oracle.build_c_oracle()
-    # the plain-C oracle is slow (scalar fp64 loops): one token per thread, one timed run each
+    # the plain-C oracle is slow (scalar fp64 loops, about 1 s per token on one core): a few
+    # tokens per thread, one timed run each
     for label, nth in (("c_all_cores", cores), ("c_one_core", 1)):
-        r = min(nth, w.N)
+        r = min(4 * nth, w.N)
         tc = _time_c(inp, r, nth)
         samples[label] = {"tokens_per_s": r / tc, "rows": r, "s": tc, "threads": nth}
     res["samples"] = samples
@@ -284,6 +305,7 @@ def run_reference(args, w):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": config_of(w, min(args.chunk, w.N) if args.chunk > 0 else 0, args),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+                             "cpu_model": cpu_model(),
                              "sample": f"{rows} tokens per step at full d and V (numpy fp64 oracle, fwd+bwd)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -466,12 +488,16 @@ def main():
     lce.profile_begin()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    t_start = time.time()
     ev0.record(stream)
     for _ in range(args.steps):
         step(H, y)
     ev1.record(stream)
     barrier()
+    t_end = time.time()
     prof = lce.profile_end()
+    time.sleep(0.2)            # the sampler's last in-region lines
+    clocks.mark(t_start, t_end)
     clk = clocks.stop()
     ms = ev0.elapsed_time(ev1)
     if world > 1:
@@ -568,7 +594,8 @@ def main():
     regime = "burst" if region_s < 1.0 else "sustained"
     peak_key = "bf16_tflops" if regime == "burst" else "bf16_tflops_sustained"
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    sm_mhz = clk.get("sm_mhz")
+    # per-clock fractions need the clock the region ran at: at least three samples inside it
+    sm_mhz = clk.get("sm_mhz") if (clk.get("samples") or 0) >= 3 else None
     # tensor-core limit at the clock the region ran at: SMs x 8192 dense bf16 flop per SM per clock
     per_clock_tflops = num_sms * 8192 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
 

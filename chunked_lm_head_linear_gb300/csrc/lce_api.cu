@@ -29,6 +29,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <functional>
 #include <mutex>
 #include <vector>
 
@@ -71,7 +72,20 @@ struct Layout {
   int64_t chunks = 0;  // number of chunks
   size_t status = 0, loss_i = 0, lse = 0, ztgt = 0, partials = 0, P = 0;
   size_t ref = 0, alpha = 0, guard = 0, Ht = 0, total = 0;
+  size_t dh_cnt = 0, dh_part = 0;  // dH part counters and part sums (backward calls)
+  int dh_ncnt = 0;                 // number of dH part counters
 };
+
+// The dH part counters and part sums of one chunk's backward launch: a counter
+// per (dH tile, CTA, epilogue warp), and, when the vocabulary is cut into more
+// than one part, one fp32 [256 x 256] sum per dH tile and part.
+void take_dh_parts(Layout& L, int64_t d, int64_t V, const std::function<size_t(size_t)>& take) {
+  const int64_t tiles = ceil_div(L.C, 256) * ceil_div(d, 256);
+  L.dh_ncnt = static_cast<int>(tiles * 8);
+  L.dh_cnt = take(sizeof(int) * static_cast<size_t>(L.dh_ncnt));
+  const int parts = lce::dh_parts_for(V);
+  if (parts > 1) L.dh_part = take(sizeof(float) * 256 * 256 * static_cast<size_t>(tiles) * static_cast<size_t>(parts));
+}
 
 int64_t chunk_of(int64_t N, const lce_opts* o) {
   int64_t C = (o && o->chunk_tokens > 0) ? o->chunk_tokens : kDefaultChunk;
@@ -101,6 +115,7 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
     L.guard = take(sizeof(int));
     L.Ht = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(d));
     L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
+    take_dh_parts(L, d, V, take);
     L.total = off;
     return L;
   }
@@ -124,7 +139,10 @@ Layout make_layout(int op, int64_t N, int64_t d, int64_t V, const lce_opts* o) {
     L.guard = take(sizeof(int) * static_cast<size_t>(L.chunks > 0 ? L.chunks : 1));
     L.Ht = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(d));
   }
-  if (bwd) L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
+  if (bwd) {
+    L.P = take(2 * static_cast<size_t>(L.C) * static_cast<size_t>(L.ldp));
+    take_dh_parts(L, d, V, take);
+  }
   L.total = off;
   return L;
 }
@@ -389,6 +407,8 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   dp.ld = c.d;
   dp.rowscale = rowscale;
   dp.st = c.st;
+  dp.part_buf = c.L.dh_part ? reinterpret_cast<float4*>(c.ws + c.L.dh_part) : nullptr;
+  dp.part_cnt = reinterpret_cast<int*>(c.ws + c.L.dh_cnt);
   lce::DwParams wp;
   wp.rows = static_cast<int>(c.V);
   wp.N = static_cast<int>(c.d);
@@ -512,9 +532,11 @@ int row_references(const Call& c) {
 int prepare(const Call& c, const float* grad_loss, bool reset_guards = true) {
   int* guards = c.L.guard ? reinterpret_cast<int*>(c.ws + c.L.guard) : nullptr;
   const int nguards = c.L.guard && reset_guards ? static_cast<int>(c.L.chunks) : 0;
+  int* cnt = c.L.dh_cnt ? reinterpret_cast<int*>(c.ws + c.L.dh_cnt) : nullptr;
+  const int ncnt = c.L.dh_cnt ? c.L.dh_ncnt : 0;
   return timed(c.s, K_PREPARE, 8.0 * static_cast<double>(c.N), [&] {
     return cuda_rc(lce::launch_prepare(c.y, c.N, static_cast<int>(c.V_total), c.o.ignore_index, c.o.reduction,
-                                       c.o.n_valid_override, grad_loss, c.st, guards, nguards, c.s));
+                                       c.o.n_valid_override, grad_loss, c.st, guards, nguards, cnt, ncnt, c.s));
   });
 }
 

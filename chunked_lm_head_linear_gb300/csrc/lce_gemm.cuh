@@ -73,9 +73,10 @@ struct PairSmemLayout {
 static_assert(PairSmemLayout::kDynamicBytes <= 232448, "shared memory budget (pair kernel)");
 
 // A tile of work: which GEMM of the problem (kind), its 256-row block, its
-// 256-column block and its number of k-blocks.
+// 256-column block, its number of k-blocks, the first of them (k-block kb0 of
+// the operands' K extent) and, for a reduction cut into parts, which part.
 struct TileJob {
-  int kind, mb, nb, k_blocks;
+  int kind, mb, nb, k_blocks, kb0, part;
 };
 
 // What an epilogue warp needs besides its tile: its staging tile, the store
@@ -151,7 +152,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 //   job(p, cluster, P, j)       its j-th tile
 //   load(p, kind, a, b, bar, m0, n0, k0)  this CTA's half of the k-block (TMA, pair form)
 //   a_desc / b_desc(kind, addr, k), idesc(kind)   MMA descriptors
-//   init(p, st), epilogue(p, st, kind, ctx, m0, col0, taddr)
+//   init(p, st), epilogue(p, st, job, ctx, m0, col0, taddr)
 template <class Prob>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ typename Prob::Params p) {
@@ -221,7 +222,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
         const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
         if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (P_A_BYTES + P_B_BYTES));
-        Prob::load(p, tj.kind, sA + stage * P_A_BYTES, sB + stage * P_B_BYTES, fbar, m0, nh, kb * BK);
+        Prob::load(p, tj.kind, sA + stage * P_A_BYTES, sB + stage * P_B_BYTES, fbar, m0, nh, (tj.kb0 + kb) * BK);
         armed |= 1u << stage;
         armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == P_STAGES) {
@@ -304,8 +305,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       for (int h = half; h < 2; h += EPI_WARPS / 4) {  // the 128-column halves this warp owns
         const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
                                static_cast<uint32_t>(acc * BN + h * EPI_COLS);
-        Prob::epilogue(p, st, tj.kind, ctx, tj.mb * P_TILE_M + static_cast<int>(rank) * 128,
-                       tj.nb * BN + h * EPI_COLS, taddr);
+        Prob::epilogue(p, st, tj, ctx, tj.mb * P_TILE_M + static_cast<int>(rank) * 128, tj.nb * BN + h * EPI_COLS,
+                       taddr);
       }
       tc_fence_before_sync();
       __syncwarp();

@@ -67,7 +67,29 @@ struct DhParams {
   long long ld;
   const float* rowscale; // optional per-row factor (nullptr: none)
   const DevStatus* st;   // gscale
+  // The K = V reduction of a dH tile runs as `parts` tiles over fixed vocabulary
+  // parts (dh_parts_for(V)); each stores its fp32 sum, and the last of them to
+  // arrive adds the parts in part order and writes the tile.
+  int parts;             // 1: one tile over the whole vocabulary
+  int tiles_n;           // 256-column blocks of d (tile index = row block * tiles_n + column block)
+  float4* part_buf;      // [tiles, parts, 2 CTAs, 4 warps, 64 column groups, 32 lanes] fp32 part sums
+  int* part_cnt;         // [tiles, 2, 4] arrivals per warp slice; zero before and after each launch
 };
+
+// dH parts: the vocabulary's k-blocks (64 words each) are cut into at most
+// kDhParts parts of ceil(kblocks / kDhParts) k-blocks. A function of V alone,
+// so that every chunk size sums dH in the same order (dH is bitwise the same
+// for every chunk size).
+constexpr int kDhParts = 4;
+inline int dh_kblocks_per_part(long long V) {
+  const long long kb = (V + 63) / 64;
+  return static_cast<int>((kb + kDhParts - 1) / kDhParts);
+}
+inline int dh_parts_for(long long V) {
+  const long long kb = (V + 63) / 64;
+  const long long per = dh_kblocks_per_part(V);
+  return per > 0 ? static_cast<int>((kb + per - 1) / per) : 1;
+}
 
 struct DwParams {
   int rows;              // V
@@ -79,9 +101,10 @@ struct DwParams {
 };
 
 // Kernel launches (return cudaGetLastError()).
+// Also zeroes guards[0, nguards) and cnt[0, ncnt) (the dH part counters).
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
                            long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
-                           cudaStream_t s);
+                           int* cnt, int ncnt, cudaStream_t s);
 // Logits GEMM of a chunk: z [M, N] = A [M, K] B [N, K]^T with the FwdEpi
 // epilogue; a, b: K-major operand maps, c: the epilogue's store map (any valid
 // map if the mode stores nothing).

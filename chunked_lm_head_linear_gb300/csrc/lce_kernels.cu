@@ -198,12 +198,104 @@ struct DhEpi {
   static __device__ __forceinline__ bool skip(const Params&) { return false; }
   static __device__ __forceinline__ void init(const Params& p, State& st) { st.g = p.st->gscale; }
 
+  // One 128-column half (col0) of a part tile: store this warp's fp32 sums of
+  // the part (32 rows x 128 columns, lane-contiguous: slot[group][lane]). After
+  // the second half the warp counts its arrival; the warp that brings the count
+  // to `parts` adds the parts' sums in part order and writes the 256 columns of
+  // the tile (so the order of the additions never depends on which part ends
+  // last). No warp waits for another.
+  static __device__ __forceinline__ void part_half(const Params& p, const EpiCtx& ctx, int m0, int col0,
+                                                   uint32_t taddr, int part, int tile, float f) {
+    const int lane = ctx.lane;
+    const int rank = (m0 % P_TILE_M) / 128;
+    const int q = ctx.row0 / 32;
+    const int h = (col0 % BN) / EPI_COLS;
+    const long long slice = (static_cast<long long>(tile) * 2 + rank) * 4 + q;  // this warp's 32 rows of the tile
+    auto slot = [&](int s) { return p.part_buf + ((slice * p.parts + s) * 64) * 32; };
+    float4* mine = slot(part);
+#pragma unroll 1
+    for (int u = 0; u < EPI_COLS / 32; ++u) {
+      float v[32];
+      tmem_ld_32x32b_x32(taddr + u * 32, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        mine[(h * 32 + u * 8 + j) * 32 + lane] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (h == 0) return;
+    // all 256 columns of this part are stored: count the arrival (release), and
+    // the last of the parts finishes the tile (acquire)
+    __threadfence();
+    __syncwarp();
+    int prior = 0;
+    if (lane == 0) {
+      __threadfence();
+      prior = atomicAdd(p.part_cnt + slice, 1);
+    }
+    prior = __shfl_sync(0xffffffffu, prior, 0);
+    if (prior != p.parts - 1) return;
+    __threadfence();
+    const int tcol0 = col0 - EPI_COLS;  // first column of the tile
+    const int groups = p.f32_out ? BN / 32 : BN / 64;
+#pragma unroll 1
+    for (int u = 0; u < groups; ++u) {
+      const int width = p.f32_out ? 32 : 64;
+      if (tcol0 + u * width >= p.N) break;
+      stage_acquire(ctx);
+#pragma unroll 1
+      for (int hh = 0; hh < width / 32; ++hh) {
+        const int g0 = (u * width + hh * 32) / 4;  // first 4-column group of these 32 columns
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 a = __ldcg(slot(0) + (g0 + j) * 32 + lane);
+          v[4 * j] = a.x;
+          v[4 * j + 1] = a.y;
+          v[4 * j + 2] = a.z;
+          v[4 * j + 3] = a.w;
+        }
+#pragma unroll 1
+        for (int s = 1; s < p.parts; ++s) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float4 a = __ldcg(slot(s) + (g0 + j) * 32 + lane);
+            v[4 * j] += a.x;
+            v[4 * j + 1] += a.y;
+            v[4 * j + 2] += a.z;
+            v[4 * j + 3] += a.w;
+          }
+        }
+        if (p.f32_out) {
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4*>(ctx.stage + stage_off(lane, q4)) =
+                make_float4(v[4 * q4] * f, v[4 * q4 + 1] * f, v[4 * q4 + 2] * f, v[4 * q4 + 3] * f);
+        } else {
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w;
+            w.x = pack_bf16x2(v[8 * q4 + 0] * f, v[8 * q4 + 1] * f);
+            w.y = pack_bf16x2(v[8 * q4 + 2] * f, v[8 * q4 + 3] * f);
+            w.z = pack_bf16x2(v[8 * q4 + 4] * f, v[8 * q4 + 5] * f);
+            w.w = pack_bf16x2(v[8 * q4 + 6] * f, v[8 * q4 + 7] * f);
+            *reinterpret_cast<uint4*>(ctx.stage + stage_off(lane, hh * 4 + q4)) = w;
+          }
+        }
+      }
+      stage_release(ctx, tcol0 + u * width, m0 + ctx.row0, false);
+    }
+    if (lane == 0) p.part_cnt[slice] = 0;  // ready for the next launch
+  }
+
   static __device__ __forceinline__ void tile(const Params& p, State& st, const EpiCtx& ctx, int m0, int col0,
-                                              uint32_t taddr) {
+                                              uint32_t taddr, int part, int tile_index) {
     const int r = m0 + ctx.row0 + ctx.lane;
     if (m0 + ctx.row0 >= p.rows) return;  // all 32 rows of this warp are past the chunk
     float f = st.g;
     if (r < p.rows && p.rowscale != nullptr) f *= p.rowscale[r];
+    if (p.parts > 1) {
+      part_half(p, ctx, m0, col0, taddr, part, tile_index, f);
+      return;
+    }
     if (p.f32_out) {  // fp32 tiles of 32 columns, like the dW epilogue
 #pragma unroll 1
       for (int u = 0; u < EPI_COLS / 32; ++u) {
@@ -277,8 +369,10 @@ struct DwEpi {
 // ----------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) k_prepare(const int64_t* __restrict__ y, long long N, int V,
                                                   long long ignore_index, int reduction, long long n_override,
-                                                  const float* grad_loss, DevStatus* st, int* guards, int nguards) {
+                                                  const float* grad_loss, DevStatus* st, int* guards, int nguards,
+                                                  int* part_cnt, int ncnt) {
   for (int i = threadIdx.x; i < nguards; i += blockDim.x) guards[i] = 0;
+  for (int i = threadIdx.x; i < ncnt; i += blockDim.x) part_cnt[i] = 0;
   __shared__ long long s_cnt[32];
   __shared__ int s_bad[32];
   long long cnt = 0;
@@ -642,7 +736,7 @@ struct LogitsProb {
   }
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const int t = c + j * P;
-    return TileJob{KIND_LOGITS, t % p.m_tiles, t / p.m_tiles, p.k_blocks};
+    return TileJob{KIND_LOGITS, t % p.m_tiles, t / p.m_tiles, p.k_blocks, 0, 0};
   }
   static __device__ __forceinline__ void load(const Params& p, int, uint8_t* a, uint8_t* b, uint32_t bar, int m0,
                                               int n0, int k0) {
@@ -653,8 +747,8 @@ struct LogitsProb {
   static __device__ __forceinline__ uint64_t b_desc(int, uint32_t addr, int k) { return desc_k_major(addr, k); }
   static __device__ __forceinline__ uint32_t idesc(int) { return idesc_bf16_f32(P_TILE_M, BN, false, false); }
   static __device__ __forceinline__ void init(const Params& p, State& st) { FwdEpi::init(p.ep, st); }
-  static __device__ __forceinline__ void epilogue(const Params& p, State& st, int, EpiCtx ctx, int m0, int col0,
-                                                  uint32_t taddr) {
+  static __device__ __forceinline__ void epilogue(const Params& p, State& st, const TileJob&, EpiCtx ctx, int m0,
+                                                  int col0, uint32_t taddr) {
     ctx.out = &p.c;
     FwdEpi::tile(p.ep, st, ctx, m0, col0, taddr);
   }
@@ -677,6 +771,7 @@ struct BwdProb {
   struct Params {
     CUtensorMap ah, bh, ch, aw, bw, cw;
     int h_m, h_n, h_k;   // dH: 256-row blocks of the chunk, 256-column blocks of d, k-blocks of V
+    int h_parts, h_kpart;  // dH tiles per (row block, column block): vocabulary parts of h_kpart k-blocks
     int w_m, w_n, w_k;   // dW: 256-row blocks of V, 256-column blocks of d, k-blocks of the chunk
     int w_t0, w_tiles;   // this launch's dW tiles: [w_t0, w_t0 + w_tiles) in (row block, column block) order
     int w_phase1;        // dW tiles dealt round-robin to every cluster (a multiple of the cluster count)
@@ -694,7 +789,7 @@ struct BwdProb {
   };
   static __device__ __forceinline__ Sched sched(const Params& p, int c, int P) {
     Sched s;
-    const int nH = p.h_m * p.h_n, nW = p.w_tiles;
+    const int nH = p.h_m * p.h_n * p.h_parts, nW = p.w_tiles;
     s.hcount = c < nH ? (nH - 1 - c) / P + 1 : 0;
     const int r = nH % P;  // clusters c < r hold one dH tile more
     s.q1 = p.w_phase1 / P;
@@ -724,15 +819,22 @@ struct BwdProb {
     const int g = tl / (nmb * G);
     const int gc = p.w_n - g * G < G ? p.w_n - g * G : G;
     const int r = tl - g * nmb * G;
-    return TileJob{KIND_DW, vb0 + r / gc, g * G + r % gc, p.w_k};
+    return TileJob{KIND_DW, vb0 + r / gc, g * G + r % gc, p.w_k, 0, 0};
   }
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const Sched s = sched(p, c, P);
     if (j < s.q1) return dw_job(p, p.w_t0 + c + j * P);
     j -= s.q1;
     if (j < s.hcount) {
-      const int t = c + j * P;
-      return p.dh_mfast ? TileJob{KIND_DH, t % p.h_m, t / p.h_m, p.h_k} : TileJob{KIND_DH, t / p.h_n, t % p.h_n, p.h_k};
+      // dH tile t: vocabulary part t / (h_m h_n) (parts slowest, so the tiles running at once
+      // share operand rows of one part), then row / column block as below
+      const int t0 = c + j * P;
+      const int per = p.h_m * p.h_n;
+      const int part = t0 / per, t = t0 - part * per;
+      const int kb0 = part * p.h_kpart;
+      const int kb = p.h_k - kb0 < p.h_kpart ? p.h_k - kb0 : p.h_kpart;
+      return p.dh_mfast ? TileJob{KIND_DH, t % p.h_m, t / p.h_m, kb, kb0, part}
+                        : TileJob{KIND_DH, t / p.h_n, t % p.h_n, kb, kb0, part};
     }
     j -= s.hcount;
     return dw_job(p, p.w_t0 + p.w_phase1 + s.li + j * s.nlight);
@@ -758,11 +860,11 @@ struct BwdProb {
     DhEpi::init(p.h, st.h);
     DwEpi::init(p.w, st.w);
   }
-  static __device__ __forceinline__ void epilogue(const Params& p, State& st, int kind, EpiCtx ctx, int m0, int col0,
-                                                  uint32_t taddr) {
-    if (kind == KIND_DH) {
+  static __device__ __forceinline__ void epilogue(const Params& p, State& st, const TileJob& tj, EpiCtx ctx, int m0,
+                                                  int col0, uint32_t taddr) {
+    if (tj.kind == KIND_DH) {
       ctx.out = &p.ch;
-      DhEpi::tile(p.h, st.h, ctx, m0, col0, taddr);
+      DhEpi::tile(p.h, st.h, ctx, m0, col0, taddr, tj.part, tj.mb * p.h_n + tj.nb);
     } else {
       ctx.out = &p.cw;
       DwEpi::tile(p.w, st.w, ctx, m0, col0, taddr);
@@ -814,6 +916,8 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   p.h_m = with_dh ? ceil_div_i(rows, P_TILE_M) : 0;
   p.h_n = ceil_div_i(d, BN);
   p.h_k = ceil_div_i(V, BK);
+  p.h_kpart = dh_kblocks_per_part(V);
+  p.h_parts = dh_parts_for(V);
   p.w_m = ceil_div_i(V, P_TILE_M);
   p.w_n = ceil_div_i(d, BN);
   p.w_k = ceil_div_i(rows, BK);
@@ -832,15 +936,17 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   p.dh_mfast = d > rows ? 1 : 0;
   p.flags = flags;
   p.h = h;
+  p.h.parts = p.h_parts;
+  p.h.tiles_n = p.h_n;
   p.w = w;
-  const long long nH = static_cast<long long>(p.h_m) * p.h_n, nW = p.w_tiles;
+  const long long nH = static_cast<long long>(p.h_m) * p.h_n * p.h_parts, nW = p.w_tiles;
   const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
   if (P <= 0) return cudaSuccess;
   // Balance: every cluster should end with the same share of the launch's time. A dH k-block (A
   // K-major, B N-major) runs in ~0.98 of a dW k-block's time (both N-major): 584 vs 594 SM cycles
   // per 64-deep k-block, measured on the Qwen3.5-2B-like head with cycle counters in the MMA issuer.
   constexpr double kDhKblockCost = 0.98;
-  const double h_cost = kDhKblockCost * p.h_k, w_cost = p.w_k;
+  const double h_cost = kDhKblockCost * p.h_kpart, w_cost = p.w_k;
   const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
   const long long hmax = (nH + P - 1) / P;
   const long long r = nH % P, nlight = r == 0 ? P : P - r;
@@ -865,8 +971,9 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
 
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
                            long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
-                           cudaStream_t s) {
-  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st, guards, nguards);
+                           int* cnt, int ncnt, cudaStream_t s) {
+  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st, guards, nguards, cnt,
+                               ncnt);
   return cudaGetLastError();
 }
 
