@@ -325,6 +325,8 @@ def config_of(w, chunk, args):
                                                else "8*V*d (logits recomputed in the shard backward)")
         if args.path == "norm":
             cfg["norm"] = "zero-centred RMSNorm of x [N, d] in front of the head (eps 1e-6)"
+        if args.path == "split":
+            cfg["flops_executed_per_token"] = "8*V*d (lce_forward, then lce_backward recomputing the logits)"
     if getattr(args, "slices", 0) > 0:
         cfg["dw_slices"] = args.slices
         cfg["sm_limit"] = args.sm_limit
@@ -352,11 +354,12 @@ def main():
                     help="finish dW in this many vocabulary slices (lce_fwd_bwd_sliced); with --gpus > 1 the "
                          "FSDP-style step: dW reduced to its row owners slice by slice on a side stream")
     ap.add_argument("--sm-limit", type=int, default=0, help="with --slices: SMs the GEMM launches may use (0 = all)")
-    ap.add_argument("--path", default="fused", choices=["fused", "norm", "vshard"],
+    ap.add_argument("--path", default="fused", choices=["fused", "norm", "vshard", "split"],
                     help="fused: lce_fwd_bwd (the metric's step); norm: final RMSNorm + LM head + CE "
                          "(lce_norm_fwd_bwd, x in place of H); vshard: the vocabulary-parallel calls with "
                          "--shards shards run in turn on one GPU (partial dH summed by torch in place of the "
-                         "all-reduce)")
+                         "all-reduce); split: lce_forward then lce_backward (the recompute path behind "
+                         "FusedLinearCrossEntropy(recompute=True), 8*N*V*d executed)")
     ap.add_argument("--shards", type=int, default=4, help="with --path vshard: number of vocabulary shards")
     ap.add_argument("--graph", action="store_true",
                     help="also time the step captured once into a CUDA graph and replayed (one GPU; reported as "
@@ -426,7 +429,17 @@ def main():
                  for r in range(args.shards)]
         vs_dH = [torch.empty((N, d), dtype=torch.float32, device=dev) for _ in range(args.shards)]
 
+    if args.path == "split":
+        ws_f = torch.empty(lce.workspace_size(lce.LCE_OP_FORWARD, N, d, V, lce.make_opts(**opts)), dtype=torch.uint8,
+                           device=dev)
+        ws_b = torch.empty(lce.workspace_size(lce.LCE_OP_BACKWARD, N, d, V, lce.make_opts(**opts)),
+                           dtype=torch.uint8, device=dev)
+
     def step(Hx, yx):
+        if args.path == "split":
+            loss, lse_s = lce.lce_forward(Hx, W, yx, workspace=ws_f, **opts)
+            dH, _ = lce.lce_backward(Hx, W, yx, lse_s, dW=dW, workspace=ws_b, **opts)
+            return loss, dH
         if args.path == "norm":
             loss, _, dx, _, _ = lce.lce_norm_fwd_bwd(Hx, w_norm, W, yx, dW=dW, workspace=ws_norm, **opts)
             return loss, dx
@@ -661,7 +674,8 @@ def main():
         **({"hbm_kernels": hbm_kernels} if hbm_kernels else {}),
         **({"cublas_logits_gemm": cublas} if cublas else {}),
         **({"graph": graph} if graph else {}),
-        "extra_device_bytes": int(ws.numel()), "unfused_logits_bytes": N * V * 4,
+        "extra_device_bytes": int(ws_f.numel() + ws_b.numel()) if args.path == "split" else int(ws.numel()),
+        "unfused_logits_bytes": N * V * 4,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, args.workload)

@@ -17,6 +17,10 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "liblce.so")
+# The bounds-checking debug build (-DLCE_CHECKS): every computed global index and
+# TMA tile coordinate is checked in the kernels; a bad one sets a device status bit.
+CHECKED_BUILD = os.path.join(BUILD, "checked")
+CHECKED_LIB = os.path.join(CHECKED_BUILD, "liblce.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr"]
@@ -48,19 +52,22 @@ def source_stamp() -> str:
     return _stamp()
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile the CUDA library if its sources changed; return its path."""
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, checks: bool = False) -> str:
+    """Compile the CUDA library if its sources changed; return its path.
+    ``checks``: the bounds-checking debug build, in its own directory."""
+    out_dir = CHECKED_BUILD if checks else BUILD
+    lib_path = CHECKED_LIB if checks else LIB
+    os.makedirs(out_dir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DLCE_CHECKS"] if checks else [])
     stamp = _stamp(extra)
-    stamp_file = os.path.join(BUILD, "liblce.stamp")
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_file)
+    stamp_file = os.path.join(out_dir, "liblce.stamp")
+    if (not force and os.path.exists(lib_path) and os.path.exists(stamp_file)
             and open(stamp_file).read() == stamp):
-        return LIB
+        return lib_path
     cc = nvcc()
     procs, objs = [], []
     for src in SOURCES:
-        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        obj = os.path.join(out_dir, src.replace(".cu", ".o"))
         objs.append(obj)
         cmd = [cc, *ARCH, *CFLAGS, *INCLUDE, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
@@ -75,14 +82,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib_path + f".{os.getpid()}.tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_path)
     with open(stamp_file, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                checks="--checks" in sys.argv))

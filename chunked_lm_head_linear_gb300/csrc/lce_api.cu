@@ -409,6 +409,7 @@ int dh_dw(const Call& c, int64_t c0, int64_t rows, const float* rowscale, const 
   dp.st = c.st;
   dp.part_buf = c.L.dh_part ? reinterpret_cast<float4*>(c.ws + c.L.dh_part) : nullptr;
   dp.part_cnt = reinterpret_cast<int*>(c.ws + c.L.dh_cnt);
+  dp.part_slices = c.L.dh_ncnt;
   lce::DwParams wp;
   wp.rows = static_cast<int>(c.V);
   wp.N = static_cast<int>(c.d);
@@ -494,7 +495,7 @@ int fused_chunk(const Call& c, int64_t chunk, int64_t c0, int64_t rows, float* l
           reinterpret_cast<const float*>(c.ws + c.L.ztgt), c.y + c0, static_cast<int>(c.V), c.o.ignore_index, ref,
           guard, lse + c0, loss_i + c0, alpha, reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp,
           reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * c.d), static_cast<int>(c.d),
-          reinterpret_cast<__nv_bfloat16*>(Ht), only_if, c.s));
+          reinterpret_cast<__nv_bfloat16*>(Ht), only_if, &c.st->flags, c.s));
     });
   };
   LCE_TRY(combine(nullptr));
@@ -550,6 +551,7 @@ int finish(const Call& c) {
   LCE_CUDA(cudaStreamSynchronize(c.s));
   int flags = 0;
   LCE_CUDA(cudaMemcpy(&flags, &c.st->flags, sizeof flags, cudaMemcpyDeviceToHost));
+  if (flags & lce::kFlagBounds) return LCE_ERR_BOUNDS;
   if (flags & lce::kFlagTimeout) return LCE_ERR_TIMEOUT;
   if (flags & lce::kFlagLabelRange) return LCE_ERR_LABEL_RANGE;
   return LCE_OK;
@@ -884,7 +886,7 @@ int lce_vshard_chunk_backward(const void* H, const void* W_shard, const int64_t*
         vocab_offset, static_cast<int>(V_shard), static_cast<int>(V_total), c.o.ignore_index,
         reinterpret_cast<const float*>(c.ws + c.L.ref), guard, lse + c0, alpha,
         reinterpret_cast<__nv_bfloat16*>(P), c.L.ldp, reinterpret_cast<const __nv_bfloat16*>(c.H + c0 * d),
-        static_cast<int>(d), reinterpret_cast<__nv_bfloat16*>(Ht), c.s));
+        static_cast<int>(d), reinterpret_cast<__nv_bfloat16*>(Ht), &c.st->flags, c.s));
   }));
   // The exact gradient tile, only if the stats call found the exp tile out of range.
   LogitsArgs g;
@@ -961,6 +963,7 @@ int lce_norm_fwd_bwd(const void* x, const float* w_norm, float eps, const void* 
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LCE_ERR_CUDA;
   int flags = 0;
   if (cudaMemcpy(&flags, base, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess) return LCE_ERR_CUDA;
+  if (flags & lce::kFlagBounds) return LCE_ERR_BOUNDS;
   if (flags & lce::kFlagTimeout) return LCE_ERR_TIMEOUT;
   if (flags & lce::kFlagLabelRange) return LCE_ERR_LABEL_RANGE;
   return LCE_OK;
@@ -998,6 +1001,7 @@ const char* lce_status_string(int status) {
     case LCE_ERR_CUDA: return "CUDA error";
     case LCE_ERR_LABEL_RANGE: return "label outside [0, V) and not ignore_index";
     case LCE_ERR_TIMEOUT: return "device wait timed out";
+    case LCE_ERR_BOUNDS: return "index outside its buffer (bounds-checked build)";
     default: return "unknown status";
   }
 }

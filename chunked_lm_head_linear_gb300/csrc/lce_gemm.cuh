@@ -86,6 +86,7 @@ struct EpiCtx {
   const CUtensorMap* out;    // TMA store / reduce map of the epilogue's output
   int lane;
   int row0;                  // first tile row of this warp (tile-relative)
+  int* flags;                // device status word (bounds bit of the checked build)
 };
 
 // Byte offset of 16-byte chunk j of row r in a 128-byte-swizzled staging tile.
@@ -104,7 +105,13 @@ __device__ __forceinline__ void stage_release(const EpiCtx& c, int x, int y, boo
   fence_proxy_async_smem();
   __syncwarp();
   if (c.lane == 0) {
-    if (reduce_add)
+    // checked build: a store box starts at a non-negative, 16-byte aligned element (x % 8 == 0
+    // covers both bf16 and fp32 outputs); otherwise the store is skipped
+    bool ok = true;
+    if constexpr (kChecks)
+      ok = in_bounds(x, 1ll << 31, c.flags) && in_bounds(y, 1ll << 31, c.flags) && in_bounds(x % 8, 1, c.flags);
+    if (!ok) {
+    } else if (reduce_add)
       tma_reduce_add_2d(c.out, c.stage, x, y);
     else
       tma_store_2d(c.out, c.stage, x, y);
@@ -150,6 +157,7 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 //   flags(p)                    device status word
 //   num_jobs(p, cluster, P)     number of tiles of this cluster (P clusters in the grid)
 //   job(p, cluster, P, j)       its j-th tile
+//   job_ok(p, job)              the tile lies inside the problem (checked build only)
 //   load(p, kind, a, b, bar, m0, n0, k0)  this CTA's half of the k-block (TMA, pair form)
 //   a_desc / b_desc(kind, addr, k), idesc(kind)   MMA descriptors
 //   init(p, st), epilogue(p, st, job, ctx, m0, col0, taddr)
@@ -212,6 +220,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bool ok = !Prob::no_loads(p);  // (timeout test: issue nothing)
     for (int j = 0; j < njobs && ok; ++j) {
       const TileJob tj = Prob::job(p, cluster, nclusters, j);
+      if (kChecks && !Prob::job_ok(p, tj)) {  // checked build: every role skips a bad tile
+        atomicOr(flags, kFlagBounds);
+        continue;
+      }
       const int m0 = tj.mb * P_TILE_M + static_cast<int>(rank) * 128;  // this CTA's A rows
       const int nh = tj.nb * BN + static_cast<int>(rank) * 128;         // this CTA's B columns
       for (int kb = 0; kb < tj.k_blocks; ++kb) {
@@ -247,6 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bool issued = false;
     for (int j = 0; j < njobs && ok; ++j) {
       const TileJob tj = Prob::job(p, cluster, nclusters, j);
+      if (kChecks && !Prob::job_ok(p, tj)) continue;
       const uint32_t idesc = Prob::idesc(tj.kind);
       if (!mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort)) {
         report_timeout(abort, flags);
@@ -290,12 +303,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     const int e = warp - EPI_WARP0;
     const int q = warp & 3;
     const int half = e >> 2;
-    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, nullptr, lane, q * 32};
+    EpiCtx ctx{staging + e * STAGE_TILE_BYTES, nullptr, lane, q * 32, flags};
     int acc = 0;
     uint32_t acc_phase = 0;
     typename Prob::State st;
     Prob::init(p, st);
     for (int j = 0; j < njobs; ++j) {
+      if (kChecks && !Prob::job_ok(p, Prob::job(p, cluster, nclusters, j))) continue;
       if (!warp_wait_cluster(&tfull[acc], acc_phase, abort, lane)) {
         if (lane == 0) report_timeout(abort, flags);
         break;

@@ -13,6 +13,29 @@ namespace lce {
 // public LCE_DEVICE_* bits).
 constexpr int kFlagLabelRange = 1;
 constexpr int kFlagTimeout = 2;
+constexpr int kFlagBounds = 4;
+
+// Bounds-checking debug build (compiled with -DLCE_CHECKS): every index a
+// kernel computes into a plain global buffer, and every tile coordinate it
+// hands to TMA, is checked before use; a bad one sets kFlagBounds in the
+// device status word and the access is skipped (nothing traps). In the normal
+// build the checks compile to nothing.
+#if defined(LCE_CHECKS)
+constexpr bool kChecks = true;
+#else
+constexpr bool kChecks = false;
+#endif
+
+// True if 0 <= i < n (always true without LCE_CHECKS).
+__device__ __forceinline__ bool in_bounds(long long i, long long n, int* flags) {
+  if constexpr (!kChecks) {
+    return true;
+  } else {
+    if (i >= 0 && i < n) return true;
+    if (flags != nullptr) atomicOr(flags, kFlagBounds);
+    return false;
+  }
+}
 
 // Device-side status block at the start of the workspace.
 struct DevStatus {
@@ -74,6 +97,7 @@ struct DhParams {
   int tiles_n;           // 256-column blocks of d (tile index = row block * tiles_n + column block)
   float4* part_buf;      // [tiles, parts, 2 CTAs, 4 warps, 64 column groups, 32 lanes] fp32 part sums
   int* part_cnt;         // [tiles, 2, 4] arrivals per warp slice; zero before and after each launch
+  long long part_slices; // counters (warp slices) the workspace holds (checked build)
 };
 
 // dH parts: the vocabulary's k-blocks (64 words each) are cut into at most
@@ -130,7 +154,7 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp,
-                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if,
+                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if, int* flags,
                                cudaStream_t s);
 // Vocabulary shards: per-row partial (max, sum-exp, target logit, has-target)
 // of this shard, and the fixed-order merge of R shards' partials.
@@ -149,7 +173,7 @@ cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const in
 cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int64_t* y, long long y_offset,
                                 int V_shard, int V_total, long long ignore_index, const float* ref, int* guard,
                                 float* lse, float* alpha, __nv_bfloat16* P, long long ldp, const __nv_bfloat16* H,
-                                int d, __nv_bfloat16* Ht, cudaStream_t s);
+                                int d, __nv_bfloat16* Ht, int* flags, cudaStream_t s);
 // Final zero-centred RMSNorm (lce_rmsnorm.cu). rmsnorm_bwd_blocks(N) partial
 // rows of d floats are the backward's scratch.
 int rmsnorm_bwd_blocks(long long N);

@@ -78,7 +78,7 @@ struct FwdEpi {
 
     if (p.mode == FWD_REF && col0 >= EPI_COLS) return;
     if (vlim <= 0) {  // this half tile lies entirely past the vocabulary
-      if (live && p.mode != FWD_REF && p.mode != FWD_GRAD)
+      if (live && p.mode != FWD_REF && p.mode != FWD_GRAD && in_bounds(part, p.nparts, p.flags))
         p.partials[static_cast<long long>(r) * p.nparts + part] = make_float2(-INFINITY, 0.f);
       return;
     }
@@ -180,7 +180,7 @@ struct FwdEpi {
       p.ref[r] = m;
       return;
     }
-    if (stats) {
+    if (stats && in_bounds(part, p.nparts, p.flags)) {
       p.partials[static_cast<long long>(r) * p.nparts + part] = make_float2(m, s);
       if (have_t) p.ztgt[r] = zt;
       if (by_ref && over) *p.guard = 1;
@@ -211,6 +211,7 @@ struct DhEpi {
     const int q = ctx.row0 / 32;
     const int h = (col0 % BN) / EPI_COLS;
     const long long slice = (static_cast<long long>(tile) * 2 + rank) * 4 + q;  // this warp's 32 rows of the tile
+    if (!in_bounds(slice, p.part_slices, ctx.flags) || !in_bounds(part, p.parts, ctx.flags)) return;
     auto slot = [&](int s) { return p.part_buf + ((slice * p.parts + s) * 64) * 32; };
     float4* mine = slot(part);
 #pragma unroll 1
@@ -468,7 +469,8 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
                                                      float* __restrict__ loss_i, float* __restrict__ alpha,
                                                      __nv_bfloat16* __restrict__ P, long long ldp,
                                                      const uint4* __restrict__ H, int groups_per_row,
-                                                     uint4* __restrict__ Ht, const int* __restrict__ only_if) {
+                                                     uint4* __restrict__ Ht, const int* __restrict__ only_if,
+                                                     int* flags) {
   if (only_if != nullptr && *only_if == 0) return;  // conditional launch whose condition is false
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
         const float rf = ref[r];
         a = exp2f((rf - l) * kLog2e);
         const float py = exp2f((ztgt[r] - rf) * kLog2e) - exp2f((l - rf) * kLog2e);
-        P[static_cast<long long>(r) * ldp + yr] = __float2bfloat16_rn(py);
+        if (in_bounds(yr, ldp, flags)) P[static_cast<long long>(r) * ldp + yr] = __float2bfloat16_rn(py);
       }
     }
     alpha[r] = a;
@@ -614,7 +616,7 @@ __global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__
                                                       const int* __restrict__ guard, const float* __restrict__ lse,
                                                       float* __restrict__ alpha, __nv_bfloat16* __restrict__ P,
                                                       long long ldp, const uint4* __restrict__ H, int groups_per_row,
-                                                      uint4* __restrict__ Ht) {
+                                                      uint4* __restrict__ Ht, int* flags) {
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -629,7 +631,7 @@ __global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__
         const float l = lse[r], rf = ref[r];
         a = exp2f((rf - l) * kLog2e);
         const long long col = yr - y_offset;
-        if (col >= 0 && col < V_shard) {
+        if (col >= 0 && col < V_shard && in_bounds(col, ldp, flags)) {
           float zt = 0.f;  // the label's logit, from the shard that holds it (this one)
           for (int k = 0; k < R; ++k) {
             const float4 q = stats[static_cast<long long>(k) * rows + r];
@@ -738,6 +740,10 @@ struct LogitsProb {
     const int t = c + j * P;
     return TileJob{KIND_LOGITS, t % p.m_tiles, t / p.m_tiles, p.k_blocks, 0, 0};
   }
+  static __device__ __forceinline__ bool job_ok(const Params& p, const TileJob& tj) {
+    return tj.kind == KIND_LOGITS && tj.mb >= 0 && tj.mb < p.m_tiles && tj.nb >= 0 && tj.nb < p.n_tiles &&
+           tj.kb0 == 0 && tj.k_blocks == p.k_blocks && tj.k_blocks > 0;
+  }
   static __device__ __forceinline__ void load(const Params& p, int, uint8_t* a, uint8_t* b, uint32_t bar, int m0,
                                               int n0, int k0) {
     load_k_major(a, &p.a, bar, m0, k0);
@@ -776,6 +782,7 @@ struct BwdProb {
     int w_t0, w_tiles;   // this launch's dW tiles: [w_t0, w_t0 + w_tiles) in (row block, column block) order
     int w_phase1;        // dW tiles dealt round-robin to every cluster (a multiple of the cluster count)
     int dh_mfast;        // dH tiles walk row blocks first (when W is larger than the chunk's exp tile)
+    int odd_dh_first;    // odd clusters take their dH tiles before their first-phase dW tiles
     int* flags;
     DhParams h;
     DwParams w;
@@ -823,21 +830,38 @@ struct BwdProb {
   }
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const Sched s = sched(p, c, P);
+    if (p.odd_dh_first && (c & 1)) {  // this cluster: dH tiles, then its first-phase dW tiles
+      if (j < s.hcount) return dh_job(p, c, P, j);
+      j -= s.hcount;
+      if (j < s.q1) return dw_job(p, p.w_t0 + c + j * P);
+      j -= s.q1;
+      return dw_job(p, p.w_t0 + p.w_phase1 + s.li + j * s.nlight);
+    }
     if (j < s.q1) return dw_job(p, p.w_t0 + c + j * P);
     j -= s.q1;
-    if (j < s.hcount) {
-      // dH tile t: vocabulary part t / (h_m h_n) (parts slowest, so the tiles running at once
-      // share operand rows of one part), then row / column block as below
-      const int t0 = c + j * P;
-      const int per = p.h_m * p.h_n;
-      const int part = t0 / per, t = t0 - part * per;
-      const int kb0 = part * p.h_kpart;
-      const int kb = p.h_k - kb0 < p.h_kpart ? p.h_k - kb0 : p.h_kpart;
-      return p.dh_mfast ? TileJob{KIND_DH, t % p.h_m, t / p.h_m, kb, kb0, part}
-                        : TileJob{KIND_DH, t / p.h_n, t % p.h_n, kb, kb0, part};
-    }
+    if (j < s.hcount) return dh_job(p, c, P, j);
     j -= s.hcount;
     return dw_job(p, p.w_t0 + p.w_phase1 + s.li + j * s.nlight);
+  }
+  // The j-th dH tile of cluster c (dealt round-robin).
+  static __device__ __forceinline__ bool job_ok(const Params& p, const TileJob& tj) {
+    if (tj.kind == KIND_DH)
+      return tj.mb >= 0 && tj.mb < p.h_m && tj.nb >= 0 && tj.nb < p.h_n && tj.part >= 0 && tj.part < p.h_parts &&
+             tj.kb0 == tj.part * p.h_kpart && tj.k_blocks > 0 && tj.kb0 + tj.k_blocks <= p.h_k;
+    const int vb0 = p.w_t0 / p.w_n;
+    return tj.kind == KIND_DW && tj.mb >= vb0 && tj.mb < vb0 + p.w_tiles / p.w_n && tj.mb < p.w_m && tj.nb >= 0 &&
+           tj.nb < p.w_n && tj.kb0 == 0 && tj.k_blocks == p.w_k && tj.k_blocks > 0;
+  }
+  // dH tile t = c + j P: vocabulary part t / (h_m h_n) (parts slowest, so the tiles running at
+  // once share operand rows of one part), then row and column block.
+  static __device__ __forceinline__ TileJob dh_job(const Params& p, int c, int P, int j) {
+    const int t0 = c + j * P;
+    const int per = p.h_m * p.h_n;
+    const int part = t0 / per, t = t0 - part * per;
+    const int kb0 = part * p.h_kpart;
+    const int kb = p.h_k - kb0 < p.h_kpart ? p.h_k - kb0 : p.h_kpart;
+    return p.dh_mfast ? TileJob{KIND_DH, t % p.h_m, t / p.h_m, kb, kb0, part}
+                      : TileJob{KIND_DH, t / p.h_n, t % p.h_n, kb, kb0, part};
   }
   static __device__ __forceinline__ void load(const Params& p, int kind, uint8_t* a, uint8_t* b, uint32_t bar,
                                               int m0, int n0, int k0) {
@@ -902,6 +926,8 @@ cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUte
   return launch_pair<LogitsProb>(p, clusters, s);
 }
 
+constexpr int kOddDhFirstMaxK = 16;  // k-blocks of a dW tile (chunks of up to 1024 rows)
+
 cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
                             const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
                             const DhParams& h, const DwParams& w, int* flags, int num_sms, cudaStream_t s,
@@ -934,6 +960,10 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   // column blocks first) or W [V, d] (walk row blocks first). On the d = 7168 head this cut the
   // dH part's DRAM reads from 24 to 15 GB per chunk.
   p.dh_mfast = d > rows ? 1 : 0;
+  // Short dW tiles (K = the chunk's rows) are dominated by their fp32 reduce-add into dW; when all
+  // clusters run them at once the launch waits on DRAM. With odd clusters taking their dH tiles
+  // first, half of the clusters run dW tiles at any time.
+  p.odd_dh_first = p.w_k <= kOddDhFirstMaxK ? 1 : 0;
   p.flags = flags;
   p.h = h;
   p.h.parts = p.h_parts;
@@ -989,14 +1019,14 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                int V, long long ignore_index, const float* ref, const int* guard, float* lse,
                                float* loss_i, float* alpha, __nv_bfloat16* P, long long ldp,
-                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if,
+                               const __nv_bfloat16* H, int d, __nv_bfloat16* Ht, const int* only_if, int* flags,
                                cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
   k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, ref, guard,
                                                        lse, loss_i, alpha, P, ldp, reinterpret_cast<const uint4*>(H),
-                                                       d / 8, reinterpret_cast<uint4*>(Ht), only_if);
+                                                       d / 8, reinterpret_cast<uint4*>(Ht), only_if, flags);
   return cudaGetLastError();
 }
 
@@ -1022,7 +1052,7 @@ cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const in
 cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int64_t* y, long long y_offset,
                                 int V_shard, int V_total, long long ignore_index, const float* ref, int* guard,
                                 float* lse, float* alpha, __nv_bfloat16* P, long long ldp, const __nv_bfloat16* H,
-                                int d, __nv_bfloat16* Ht, cudaStream_t s) {
+                                int d, __nv_bfloat16* Ht, int* flags, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   k_vshard_lse<<<(rows + 255) / 256, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
                                                   guard, lse);
@@ -1030,7 +1060,7 @@ cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int6
   if (e != cudaSuccess) return e;
   k_vshard_scale<<<(rows + 7) / 8, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
                                                 guard, lse, alpha, P, ldp, reinterpret_cast<const uint4*>(H), d / 8,
-                                                reinterpret_cast<uint4*>(Ht));
+                                                reinterpret_cast<uint4*>(Ht), flags);
   return cudaGetLastError();
 }
 

@@ -33,11 +33,12 @@ LCE_ERR_UNSUPPORTED_DEVICE = 4
 LCE_ERR_CUDA = 5
 LCE_ERR_LABEL_RANGE = 6
 LCE_ERR_TIMEOUT = 7
+LCE_ERR_BOUNDS = 8
 
 LCE_MEAN, LCE_SUM = 0, 1
 LCE_OP_FORWARD, LCE_OP_BACKWARD, LCE_OP_FWD_BWD, LCE_OP_VSHARD_COMBINE, LCE_OP_NORM_FWD_BWD = 0, 1, 2, 3, 4
 LCE_OP_VSHARD_CHUNK = 5
-LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT = 1, 2
+LCE_DEVICE_LABEL_RANGE, LCE_DEVICE_TIMEOUT, LCE_DEVICE_BOUNDS = 1, 2, 4
 LCE_TEST_FORCE_TIMEOUT = 0x7E57
 
 # Every symbol include/lce.h declares.

@@ -64,6 +64,9 @@ extern "C" {
 #define LCE_ERR_CUDA 5               /* a CUDA runtime / driver call failed */
 #define LCE_ERR_LABEL_RANGE 6        /* a label is neither ignore_index nor in [0, V) */
 #define LCE_ERR_TIMEOUT 7            /* a device-side wait exceeded its limit */
+#define LCE_ERR_BOUNDS 8             /* (a library built with LCE_CHECKS only) a kernel computed an
+                                        index or tile coordinate outside its buffer; the access
+                                        was skipped, so the outputs are not valid */
 
 /* reductions */
 #define LCE_MEAN 0
@@ -80,6 +83,7 @@ extern "C" {
 /* device status bits returned by lce_read_device_status */
 #define LCE_DEVICE_LABEL_RANGE 1
 #define LCE_DEVICE_TIMEOUT 2
+#define LCE_DEVICE_BOUNDS 4   /* set only by a library built with LCE_CHECKS (see LCE_ERR_BOUNDS) */
 
 typedef struct lce_opts {
   int64_t chunk_tokens;     /* tokens per chunk; 0 = automatic (4096, capped at N) */

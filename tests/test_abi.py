@@ -45,7 +45,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_status_strings(lib):
     assert lib.lce_version() == 1
-    for code in range(8):
+    for code in range(9):
         s = lce.status_string(code)
         assert s and s != "unknown status"
     assert lce.status_string(99) == "unknown status"
