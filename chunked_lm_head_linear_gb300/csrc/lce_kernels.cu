@@ -783,6 +783,8 @@ struct BwdProb {
     int w_phase1;        // dW tiles dealt round-robin to every cluster (a multiple of the cluster count)
     int dh_mfast;        // dH tiles walk row blocks first (when W is larger than the chunk's exp tile)
     int odd_dh_first;    // odd clusters take their dH tiles before their first-phase dW tiles
+    int h_group;         // dH part tiles dealt together: 1 (each part on its own), or h_parts (the
+                         // parts of one 256 x 256 block back to back on one cluster)
     int* flags;
     DhParams h;
     DwParams w;
@@ -794,11 +796,20 @@ struct BwdProb {
   struct Sched {
     int hcount, q1, li, nlight, count2;
   };
+  // Position of cluster c in the dealing order. Normally c itself; when odd clusters take their
+  // dH tiles first, the even clusters come first and then the odd ones, so that the tiles dealt
+  // next to each other (which share operand blocks: the dH tiles of one W block, the dW tiles of
+  // one exp-tile block) go to clusters of the same parity and so run at the same time.
+  static __device__ __forceinline__ int deal_rank(const Params& p, int c, int P) {
+    if (!p.odd_dh_first) return c;
+    return (c & 1) ? (P + 1) / 2 + c / 2 : c / 2;
+  }
   static __device__ __forceinline__ Sched sched(const Params& p, int c, int P) {
     Sched s;
-    const int nH = p.h_m * p.h_n * p.h_parts, nW = p.w_tiles;
-    s.hcount = c < nH ? (nH - 1 - c) / P + 1 : 0;
-    const int r = nH % P;  // clusters c < r hold one dH tile more
+    c = deal_rank(p, c, P);
+    const int nH = p.h_m * p.h_n * p.h_parts / p.h_group, nW = p.w_tiles;  // dH units dealt
+    s.hcount = (c < nH ? (nH - 1 - c) / P + 1 : 0) * p.h_group;
+    const int r = nH % P;  // clusters c < r hold one dH unit more
     s.q1 = p.w_phase1 / P;
     s.nlight = r == 0 ? P : P - r;
     s.li = r == 0 ? c : c - r;
@@ -830,20 +841,20 @@ struct BwdProb {
   }
   static __device__ __forceinline__ TileJob job(const Params& p, int c, int P, int j) {
     const Sched s = sched(p, c, P);
+    const int k = deal_rank(p, c, P);
     if (p.odd_dh_first && (c & 1)) {  // this cluster: dH tiles, then its first-phase dW tiles
-      if (j < s.hcount) return dh_job(p, c, P, j);
+      if (j < s.hcount) return dh_job(p, k, P, j);
       j -= s.hcount;
-      if (j < s.q1) return dw_job(p, p.w_t0 + c + j * P);
+      if (j < s.q1) return dw_job(p, p.w_t0 + k + j * P);
       j -= s.q1;
       return dw_job(p, p.w_t0 + p.w_phase1 + s.li + j * s.nlight);
     }
-    if (j < s.q1) return dw_job(p, p.w_t0 + c + j * P);
+    if (j < s.q1) return dw_job(p, p.w_t0 + k + j * P);
     j -= s.q1;
-    if (j < s.hcount) return dh_job(p, c, P, j);
+    if (j < s.hcount) return dh_job(p, k, P, j);
     j -= s.hcount;
     return dw_job(p, p.w_t0 + p.w_phase1 + s.li + j * s.nlight);
   }
-  // The j-th dH tile of cluster c (dealt round-robin).
   static __device__ __forceinline__ bool job_ok(const Params& p, const TileJob& tj) {
     if (tj.kind == KIND_DH)
       return tj.mb >= 0 && tj.mb < p.h_m && tj.nb >= 0 && tj.nb < p.h_n && tj.part >= 0 && tj.part < p.h_parts &&
@@ -852,12 +863,15 @@ struct BwdProb {
     return tj.kind == KIND_DW && tj.mb >= vb0 && tj.mb < vb0 + p.w_tiles / p.w_n && tj.mb < p.w_m && tj.nb >= 0 &&
            tj.nb < p.w_n && tj.kb0 == 0 && tj.k_blocks == p.w_k && tj.k_blocks > 0;
   }
-  // dH tile t = c + j P: vocabulary part t / (h_m h_n) (parts slowest, so the tiles running at
-  // once share operand rows of one part), then row and column block.
-  static __device__ __forceinline__ TileJob dh_job(const Params& p, int c, int P, int j) {
-    const int t0 = c + j * P;
+  // The j-th dH tile of the cluster at dealing position k. Dealt one part at a time, unit
+  // u = k + j P is part u / (h_m h_n) (parts slowest, so the tiles running at once share operand
+  // rows of one part) of block u mod (h_m h_n); dealt a block at a time, unit u = k + (j / parts) P
+  // is block u and the cluster runs its parts in order.
+  static __device__ __forceinline__ TileJob dh_job(const Params& p, int k, int P, int j) {
+    const int u = k + (j / p.h_group) * P;
     const int per = p.h_m * p.h_n;
-    const int part = t0 / per, t = t0 - part * per;
+    const int part = p.h_group == 1 ? u / per : j % p.h_group;
+    const int t = p.h_group == 1 ? u - part * per : u;
     const int kb0 = part * p.h_kpart;
     const int kb = p.h_k - kb0 < p.h_kpart ? p.h_k - kb0 : p.h_kpart;
     return p.dh_mfast ? TileJob{KIND_DH, t % p.h_m, t / p.h_m, kb, kb0, part}
@@ -927,6 +941,7 @@ cudaError_t launch_logits(const CUtensorMap& a, const CUtensorMap& b, const CUte
 }
 
 constexpr int kOddDhFirstMaxK = 16;  // k-blocks of a dW tile (chunks of up to 1024 rows)
+constexpr double kDhBlockMaxShare = 1.25;
 
 cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const CUtensorMap& ch, const CUtensorMap& aw,
                             const CUtensorMap& bw, const CUtensorMap& cw, long long rows, long long V, long long d,
@@ -969,14 +984,24 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   p.h.parts = p.h_parts;
   p.h.tiles_n = p.h_n;
   p.w = w;
-  const long long nH = static_cast<long long>(p.h_m) * p.h_n * p.h_parts, nW = p.w_tiles;
-  const int P = static_cast<int>(nH + nW < num_sms / 2 ? nH + nW : num_sms / 2);
+  const long long nParts = static_cast<long long>(p.h_m) * p.h_n * p.h_parts, nW = p.w_tiles;
+  const int P = static_cast<int>(nParts + nW < num_sms / 2 ? nParts + nW : num_sms / 2);
   if (P <= 0) return cudaSuccess;
   // Balance: every cluster should end with the same share of the launch's time. A dH k-block (A
   // K-major, B N-major) runs in ~0.98 of a dW k-block's time (both N-major): 584 vs 594 SM cycles
   // per 64-deep k-block, measured on the Qwen3.5-2B-like head with cycle counters in the MMA issuer.
   constexpr double kDhKblockCost = 0.98;
-  const double h_cost = kDhKblockCost * p.h_kpart, w_cost = p.w_k;
+  const double w_cost = p.w_k;
+  // The parts of a dH block go to one cluster back to back when the whole block is no longer than
+  // kDhBlockMaxShare of a cluster's fair share: the blocks then run side by side on some clusters,
+  // each W and exp-tile block read by all the tiles that need it at once, while the other clusters
+  // stream the dW tiles (A/B on one box, Qwen3.5-2B-like head: 784K vs 755K tokens/s at 1024-token
+  // chunks, equal at 2048 and 4096). Otherwise the parts are dealt one by one, which balances the
+  // clusters when the blocks are fewer than them (540K vs 470K tokens/s at 512-token chunks).
+  const double fair = (static_cast<double>(nParts) * kDhKblockCost * p.h_kpart + static_cast<double>(nW) * w_cost) / P;
+  p.h_group = (p.h_parts > 1 && kDhKblockCost * p.h_k <= kDhBlockMaxShare * fair) ? p.h_parts : 1;
+  const long long nH = nParts / p.h_group;
+  const double h_cost = kDhKblockCost * (p.h_group == 1 ? p.h_kpart : p.h_k);
   const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
   const long long hmax = (nH + P - 1) / P;
   const long long r = nH % P, nlight = r == 0 ? P : P - r;
