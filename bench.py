@@ -607,8 +607,10 @@ def main():
     regime = "burst" if region_s < 1.0 else "sustained"
     peak_key = "bf16_tflops" if regime == "burst" else "bf16_tflops_sustained"
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    # per-clock fractions need the clock the region ran at: at least three samples inside it
-    sm_mhz = clk.get("sm_mhz") if (clk.get("samples") or 0) >= 3 else None
+    # per-clock fractions need the clock the region ran at: at least three samples inside a region
+    # of at least a second (in shorter regions nvidia-smi's clock and power readings lag the
+    # board: power.draw averages over about a second)
+    sm_mhz = clk.get("sm_mhz") if (clk.get("samples") or 0) >= 3 and region_s >= 1.0 else None
     # tensor-core limit at the clock the region ran at: SMs x 8192 dense bf16 flop per SM per clock
     per_clock_tflops = num_sms * 8192 * sm_mhz * 1e6 / 1e12 if sm_mhz else None
 
