@@ -11,6 +11,11 @@ uniform labels, 5% ignored at packed-document starts, seed 0).
 
 Prints ONE JSON line (rank 0). Metric: tokens/s of the fused fwd+bwd, with
 TFLOP/s counted as 6*N*V*d per step and its fraction of the dense bf16 peak.
+``roofline`` holds the dominant kernel (events around every library launch on
+its stream) against the measured burst peak when the timed region is under a
+second and the sustained one otherwise; ``gemm_kernels`` gives both GEMM
+kinds' fractions of both peaks and, for regions of a second or more, of the
+tensor-core limit at the sampled SM clock (``frac_per_clock``).
 ``value`` is device-resident throughput; ``e2e`` repeats it through the same
 public call with the step's inputs copied from pinned host memory and the
 loss read back every step. Inputs (W 0.62 GB, dW 1.24 GB, gradient tiles
