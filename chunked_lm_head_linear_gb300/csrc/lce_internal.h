@@ -98,6 +98,7 @@ struct DhParams {
   float4* part_buf;      // [tiles, parts, 2 CTAs, 4 warps, 64 column groups, 32 lanes] fp32 part sums
   int* part_cnt;         // [tiles, 2, 4] arrivals per warp slice; zero before and after each launch
   long long part_slices; // counters (warp slices) the workspace holds (checked build)
+  int block_major;       // the parts of each block run back to back on one cluster, in part order
 };
 
 // dH parts: the vocabulary's k-blocks (64 words each) are cut into at most

@@ -204,6 +204,11 @@ struct DhEpi {
   // to `parts` adds the parts' sums in part order and writes the 256 columns of
   // the tile (so the order of the additions never depends on which part ends
   // last). No warp waits for another.
+  // When a block's parts run back to back on one cluster (block_major), the
+  // same thread handles every part of its rows, in part order: the last part is
+  // known in advance, keeps its own sum in TMEM (no store) and needs no count,
+  // and the earlier parts' sums are this thread's own earlier stores. The
+  // additions are the same, in the same order.
   static __device__ __forceinline__ void part_half(const Params& p, const EpiCtx& ctx, int m0, int col0,
                                                    uint32_t taddr, int part, int tile, float f) {
     const int lane = ctx.lane;
@@ -213,29 +218,38 @@ struct DhEpi {
     const long long slice = (static_cast<long long>(tile) * 2 + rank) * 4 + q;  // this warp's 32 rows of the tile
     if (!in_bounds(slice, p.part_slices, ctx.flags) || !in_bounds(part, p.parts, ctx.flags)) return;
     auto slot = [&](int s) { return p.part_buf + ((slice * p.parts + s) * 64) * 32; };
-    float4* mine = slot(part);
+    const bool last_in_order = p.block_major && part == p.parts - 1;
+    if (!last_in_order) {
+      float4* mine = slot(part);
 #pragma unroll 1
-    for (int u = 0; u < EPI_COLS / 32; ++u) {
-      float v[32];
-      tmem_ld_32x32b_x32(taddr + u * 32, v);
+      for (int u = 0; u < EPI_COLS / 32; ++u) {
+        float v[32];
+        tmem_ld_32x32b_x32(taddr + u * 32, v);
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        mine[(h * 32 + u * 8 + j) * 32 + lane] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        for (int j = 0; j < 8; ++j)
+          mine[(h * 32 + u * 8 + j) * 32 + lane] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
     }
     if (h == 0) return;
-    // all 256 columns of this part are stored: count the arrival (release), and
-    // the last of the parts finishes the tile (acquire)
-    __threadfence();
-    __syncwarp();
-    int prior = 0;
-    if (lane == 0) {
+    if (p.block_major) {
+      if (!last_in_order) return;
+    } else {
+      // all 256 columns of this part are stored: count the arrival (release), and
+      // the last of the parts finishes the tile (acquire)
       __threadfence();
-      prior = atomicAdd(p.part_cnt + slice, 1);
+      __syncwarp();
+      int prior = 0;
+      if (lane == 0) {
+        __threadfence();
+        prior = atomicAdd(p.part_cnt + slice, 1);
+      }
+      prior = __shfl_sync(0xffffffffu, prior, 0);
+      if (prior != p.parts - 1) return;
+      __threadfence();
     }
-    prior = __shfl_sync(0xffffffffu, prior, 0);
-    if (prior != p.parts - 1) return;
-    __threadfence();
-    const int tcol0 = col0 - EPI_COLS;  // first column of the tile
+    const int tcol0 = col0 - EPI_COLS;                              // first column of the tile
+    const uint32_t ttile = taddr - static_cast<uint32_t>(EPI_COLS);  // its TMEM columns
+    const int from_mem = last_in_order ? p.parts - 1 : p.parts;     // parts whose sums are in memory
     const int groups = p.f32_out ? BN / 32 : BN / 64;
 #pragma unroll 1
     for (int u = 0; u < groups; ++u) {
@@ -255,7 +269,7 @@ struct DhEpi {
           v[4 * j + 3] = a.w;
         }
 #pragma unroll 1
-        for (int s = 1; s < p.parts; ++s) {
+        for (int s = 1; s < from_mem; ++s) {
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             const float4 a = __ldcg(slot(s) + (g0 + j) * 32 + lane);
@@ -264,6 +278,12 @@ struct DhEpi {
             v[4 * j + 2] += a.z;
             v[4 * j + 3] += a.w;
           }
+        }
+        if (last_in_order) {  // the last part's own sum, still in TMEM, added last
+          float w[32];
+          tmem_ld_32x32b_x32(ttile + static_cast<uint32_t>(u * width + hh * 32), w);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] += w[c];
         }
         if (p.f32_out) {
 #pragma unroll
@@ -284,7 +304,7 @@ struct DhEpi {
       }
       stage_release(ctx, tcol0 + u * width, m0 + ctx.row0, false);
     }
-    if (lane == 0) p.part_cnt[slice] = 0;  // ready for the next launch
+    if (!p.block_major && lane == 0) p.part_cnt[slice] = 0;  // ready for the next launch
   }
 
   static __device__ __forceinline__ void tile(const Params& p, State& st, const EpiCtx& ctx, int m0, int col0,
@@ -983,6 +1003,7 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   p.h = h;
   p.h.parts = p.h_parts;
   p.h.tiles_n = p.h_n;
+  p.h.block_major = 0;  // set below with the dealing
   p.w = w;
   const long long nParts = static_cast<long long>(p.h_m) * p.h_n * p.h_parts, nW = p.w_tiles;
   const int P = static_cast<int>(nParts + nW < num_sms / 2 ? nParts + nW : num_sms / 2);
@@ -1000,6 +1021,7 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
   // clusters when the blocks are fewer than them (540K vs 470K tokens/s at 512-token chunks).
   const double fair = (static_cast<double>(nParts) * kDhKblockCost * p.h_kpart + static_cast<double>(nW) * w_cost) / P;
   p.h_group = (p.h_parts > 1 && kDhKblockCost * p.h_k <= kDhBlockMaxShare * fair) ? p.h_parts : 1;
+  p.h.block_major = p.h_group > 1 ? 1 : 0;
   const long long nH = nParts / p.h_group;
   const double h_cost = kDhKblockCost * (p.h_group == 1 ? p.h_kpart : p.h_k);
   const double target = (static_cast<double>(nH) * h_cost + static_cast<double>(nW) * w_cost) / P;
