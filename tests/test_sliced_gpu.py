@@ -44,6 +44,9 @@ CASES = [
     (513, 264, 4099, 200, [0, 0, 256, 256, 3840, 4099], 5, 16),
     (1000, 512, 4096, 256, None, 16, 7),
     (64, 2048, 151936, 0, None, 8, 0),
+    # 1024-token chunks: the whole launches deal each dH block's four parts to one cluster, the last
+    # slice's launch (an eighth of the dW tiles) deals them one by one; same arithmetic either way
+    (2048, 2048, 151936, 1024, None, 8, 0),
 ]
 
 
