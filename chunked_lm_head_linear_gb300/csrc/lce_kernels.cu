@@ -448,6 +448,25 @@ __device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2)
   m = M;
 }
 
+// A lane's running (max, sum-exp) over its row's partials t = lane, lane + 32,
+// lane + 64, ... in that order. Eight loads are issued before their merges, so
+// a warp waits for memory once per eight partials instead of once per partial;
+// entries past T merge as (-inf, 0), which leaves (m, s) exactly unchanged, so
+// the result is that of the plain one-at-a-time loop bit for bit.
+__device__ __forceinline__ void lane_partials(const float2* __restrict__ pr, int T, int lane, float& m, float& s) {
+  constexpr int kBatch = 8;
+  for (int t0 = lane; t0 < T; t0 += 32 * kBatch) {
+    float2 q[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int t = t0 + 32 * k;
+      q[k] = t < T ? pr[t] : make_float2(-INFINITY, 0.f);
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) merge_ms(m, s, q[k].x, q[k].y);
+  }
+}
+
 // One warp per row: combine the row's vocabulary-tile partials in a fixed
 // order, lse = m + log s, loss_i = lse - z_y for valid rows (else 0).
 __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ partials, int T, int rows,
@@ -459,10 +478,7 @@ __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ part
   if (r >= rows) return;
   float m = -INFINITY, s = 0.f;
   const float2* pr = partials + static_cast<long long>(r) * T;
-  for (int t = lane; t < T; t += 32) {
-    const float2 q = pr[t];
-    merge_ms(m, s, q.x, q.y);
-  }
+  lane_partials(pr, T, lane, m, s);
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
@@ -495,12 +511,13 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
+  // the row's scalars, loaded before the partials so that their latency overlaps the merge
+  const long long yr = y[r];
+  const float zt = ztgt[r], rf = ref[r];
+  const int gd = *guard;
   float m = -INFINITY, s = 0.f;
   const float2* pr = partials + static_cast<long long>(r) * T;
-  for (int t = lane; t < T; t += 32) {
-    const float2 q = pr[t];
-    merge_ms(m, s, q.x, q.y);
-  }
+  lane_partials(pr, T, lane, m, s);
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
@@ -510,16 +527,14 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
   if (lane == 0) {
     const float l = m + logf(s);
     lse[r] = l;
-    const long long yr = y[r];
     const bool valid = yr != ignore_index && yr >= 0 && yr < V;
-    loss_i[r] = valid ? l - ztgt[r] : 0.f;
+    loss_i[r] = valid ? l - zt : 0.f;
     if (valid) {
-      if (*guard != 0) {
+      if (gd != 0) {
         a = 1.f;
       } else {
-        const float rf = ref[r];
         a = exp2f((rf - l) * kLog2e);
-        const float py = exp2f((ztgt[r] - rf) * kLog2e) - exp2f((l - rf) * kLog2e);
+        const float py = exp2f((zt - rf) * kLog2e) - exp2f((l - rf) * kLog2e);
         if (in_bounds(yr, ldp, flags)) P[static_cast<long long>(r) * ldp + yr] = __float2bfloat16_rn(py);
       }
     }
@@ -529,6 +544,7 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
   a = __shfl_sync(0xffffffffu, a, 0);
   const uint4* hr = H + static_cast<long long>(r) * groups_per_row;
   uint4* tr = Ht + static_cast<long long>(r) * groups_per_row;
+#pragma unroll 4
   for (int g = lane; g < groups_per_row; g += 32) {
     const uint4 h = hr[g];
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
@@ -554,10 +570,7 @@ __global__ void __launch_bounds__(256) k_shard_stats(const float2* __restrict__ 
   if (r >= rows) return;
   float m = -INFINITY, s = 0.f;
   const float2* pr = partials + static_cast<long long>(r) * T;
-  for (int t = lane; t < T; t += 32) {
-    const float2 q = pr[t];
-    merge_ms(m, s, q.x, q.y);
-  }
+  lane_partials(pr, T, lane, m, s);
   for (int off = 16; off > 0; off >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, off);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, off);
@@ -667,6 +680,7 @@ __global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__
   a = __shfl_sync(0xffffffffu, a, 0);
   const uint4* hr = H + static_cast<long long>(r) * groups_per_row;
   uint4* tr = Ht + static_cast<long long>(r) * groups_per_row;
+#pragma unroll 4
   for (int g = lane; g < groups_per_row; g += 32) {
     const uint4 h = hr[g];
     const uint32_t w[4] = {h.x, h.y, h.z, h.w};
