@@ -164,6 +164,8 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
 template <class Prob>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ typename Prob::Params p) {
+  grid_dep_wait();    // everything below reads or writes what earlier kernels of the stream touch
+  grid_dep_launch();
   if (Prob::skip(p)) return;  // same value in both CTAs of the pair (one global word)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);

@@ -6,8 +6,37 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
+#include <utility>
 
 namespace lce {
+
+// Programmatic dependent launch. Every kernel of the library starts with
+// grid_dep_wait(): it returns once the grids it depends on (the previous
+// kernel of the stream) have completed and their writes are visible, at once
+// when the launch did not ask for programmatic serialization. grid_dep_launch()
+// then lets the next kernel of the stream be scheduled; that kernel's own wait
+// still holds its work back until this one has completed.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Every kernel of the library goes out with programmatic stream serialization,
+// so that its launch and the scheduling of its blocks overlap the end of the
+// kernel before it in the stream (its grid_dep_wait keeps the order).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Device status bits (the workspace's flag word; the first two equal the
 // public LCE_DEVICE_* bits).

@@ -392,6 +392,8 @@ __global__ void __launch_bounds__(1024) k_prepare(const int64_t* __restrict__ y,
                                                   long long ignore_index, int reduction, long long n_override,
                                                   const float* grad_loss, DevStatus* st, int* guards, int nguards,
                                                   int* part_cnt, int ncnt) {
+  grid_dep_wait();
+  grid_dep_launch();
   for (int i = threadIdx.x; i < nguards; i += blockDim.x) guards[i] = 0;
   for (int i = threadIdx.x; i < ncnt; i += blockDim.x) part_cnt[i] = 0;
   __shared__ long long s_cnt[32];
@@ -473,6 +475,8 @@ __global__ void __launch_bounds__(256) k_combine(const float2* __restrict__ part
                                                  const float* __restrict__ ztgt, const int64_t* __restrict__ y,
                                                  int V, long long ignore_index, float* __restrict__ lse,
                                                  float* __restrict__ loss_i) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -507,6 +511,8 @@ __global__ void __launch_bounds__(256) k_combine_exp(const float2* __restrict__ 
                                                      const uint4* __restrict__ H, int groups_per_row,
                                                      uint4* __restrict__ Ht, const int* __restrict__ only_if,
                                                      int* flags) {
+  grid_dep_wait();
+  grid_dep_launch();
   if (only_if != nullptr && *only_if == 0) return;  // conditional launch whose condition is false
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
@@ -565,6 +571,8 @@ __global__ void __launch_bounds__(256) k_shard_stats(const float2* __restrict__ 
                                                      const float* __restrict__ ztgt, const int64_t* __restrict__ y,
                                                      long long y_offset, int V_shard, int V_total,
                                                      long long ignore_index, float4* __restrict__ stats) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -592,6 +600,8 @@ __global__ void __launch_bounds__(256) k_shard_merge(const float4* __restrict__ 
                                                      const int64_t* __restrict__ y, int V_total,
                                                      long long ignore_index, float* __restrict__ lse,
                                                      float* __restrict__ loss_i) {
+  grid_dep_wait();
+  grid_dep_launch();
   const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
   if (i >= N) return;
   float M = -INFINITY;
@@ -620,6 +630,8 @@ __global__ void __launch_bounds__(256) k_vshard_lse(const float4* __restrict__ s
                                                     const int64_t* __restrict__ y, long long y_offset, int V_shard,
                                                     int V_total, long long ignore_index, const float* __restrict__ ref,
                                                     int* __restrict__ guard, float* __restrict__ lse) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = static_cast<int>(blockIdx.x * blockDim.x + threadIdx.x);
   if (r >= rows) return;
   float M = -INFINITY;
@@ -650,6 +662,8 @@ __global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__
                                                       float* __restrict__ alpha, __nv_bfloat16* __restrict__ P,
                                                       long long ldp, const uint4* __restrict__ H, int groups_per_row,
                                                       uint4* __restrict__ Ht, int* flags) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int r = static_cast<int>((blockIdx.x * static_cast<unsigned>(blockDim.x) + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -696,6 +710,8 @@ __global__ void __launch_bounds__(256) k_vshard_scale(const float4* __restrict__
 // nothing is read or written when g == 1.
 __global__ void __launch_bounds__(256) k_scale(uint4* __restrict__ bf, long long nbf8, float4* __restrict__ f32,
                                                long long nf4, const float* __restrict__ gptr) {
+  grid_dep_wait();
+  grid_dep_launch();
   const float g = *gptr;
   if (g == 1.f) return;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
@@ -721,6 +737,8 @@ __global__ void __launch_bounds__(256) k_scale(uint4* __restrict__ bf, long long
 // loss = (sum_i loss_i) * lscale, fp64 accumulation in a fixed order.
 __global__ void __launch_bounds__(1024) k_finalize(const float* __restrict__ loss_i, long long N,
                                                    const DevStatus* st, float* loss) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ double red[1024];
   double acc = 0.0;
   for (long long i = threadIdx.x; i < N; i += blockDim.x) acc += static_cast<double>(loss_i[i]);
@@ -951,8 +969,7 @@ static cudaError_t launch_pair(const typename Prob::Params& p, int clusters, cud
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmemLayout::kDynamicBytes);
   if (e != cudaSuccess) return e;
-  kern<<<2 * clusters, NUM_THREADS, PairSmemLayout::kDynamicBytes, s>>>(p);
-  return cudaGetLastError();
+  return launch_k(kern, 2 * clusters, NUM_THREADS, PairSmemLayout::kDynamicBytes, s, p);
 }
 
 static int ceil_div_i(long long a, long long b) { return static_cast<int>((a + b - 1) / b); }
@@ -1063,9 +1080,8 @@ cudaError_t launch_backward(const CUtensorMap& ah, const CUtensorMap& bh, const 
 cudaError_t launch_prepare(const int64_t* y, long long N, int V, long long ignore_index, int reduction,
                            long long n_override, const float* grad_loss, DevStatus* st, int* guards, int nguards,
                            int* cnt, int ncnt, cudaStream_t s) {
-  k_prepare<<<1, 1024, 0, s>>>(y, N, V, ignore_index, reduction, n_override, grad_loss, st, guards, nguards, cnt,
-                               ncnt);
-  return cudaGetLastError();
+  return launch_k(k_prepare, 1, 1024, 0, s, y, N, V, ignore_index, reduction, n_override, grad_loss, st, guards,
+                  nguards, cnt, ncnt);
 }
 
 cudaError_t launch_combine(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
@@ -1073,8 +1089,8 @@ cudaError_t launch_combine(const float2* partials, int nparts, int rows, const f
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  k_combine<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, lse, loss_i);
-  return cudaGetLastError();
+  return launch_k(k_combine, grid, 32 * warps_per_block, 0, s, partials, nparts, rows, ztgt, y, V, ignore_index, lse,
+                  loss_i);
 }
 
 cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
@@ -1085,29 +1101,26 @@ cudaError_t launch_combine_exp(const float2* partials, int nparts, int rows, con
   if (rows <= 0) return cudaSuccess;
   const int warps_per_block = 8;
   const int grid = (rows + warps_per_block - 1) / warps_per_block;
-  k_combine_exp<<<grid, 32 * warps_per_block, 0, s>>>(partials, nparts, rows, ztgt, y, V, ignore_index, ref, guard,
-                                                       lse, loss_i, alpha, P, ldp, reinterpret_cast<const uint4*>(H),
-                                                       d / 8, reinterpret_cast<uint4*>(Ht), only_if, flags);
-  return cudaGetLastError();
+  return launch_k(k_combine_exp, grid, 32 * warps_per_block, 0, s, partials, nparts, rows, ztgt, y, V, ignore_index,
+                  ref, guard, lse, loss_i, alpha, P, ldp, reinterpret_cast<const uint4*>(H), d / 8,
+                  reinterpret_cast<uint4*>(Ht), only_if, flags);
 }
-
 
 cudaError_t launch_shard_stats(const float2* partials, int nparts, int rows, const float* ztgt, const int64_t* y,
                                long long y_offset, int V_shard, int V_total, long long ignore_index, float4* stats,
                                cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
   const int grid = (rows + 7) / 8;
-  k_shard_stats<<<grid, 256, 0, s>>>(partials, nparts, rows, ztgt, y, y_offset, V_shard, V_total, ignore_index,
-                                     stats);
-  return cudaGetLastError();
+  return launch_k(k_shard_stats, grid, 256, 0, s, partials, nparts, rows, ztgt, y, y_offset, V_shard, V_total,
+                  ignore_index, stats);
 }
 
 cudaError_t launch_shard_merge(const float4* stats, int R, long long N, const int64_t* y, int V_total,
                                long long ignore_index, float* lse, float* loss_i, cudaStream_t s) {
   if (N <= 0) return cudaSuccess;
   const long long grid = (N + 255) / 256;
-  k_shard_merge<<<static_cast<unsigned>(grid), 256, 0, s>>>(stats, R, N, y, V_total, ignore_index, lse, loss_i);
-  return cudaGetLastError();
+  return launch_k(k_shard_merge, static_cast<unsigned>(grid), 256, 0, s, stats, R, N, y, V_total, ignore_index, lse,
+                  loss_i);
 }
 
 cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int64_t* y, long long y_offset,
@@ -1115,27 +1128,23 @@ cudaError_t launch_vshard_scale(const float4* stats, int R, int rows, const int6
                                 float* lse, float* alpha, __nv_bfloat16* P, long long ldp, const __nv_bfloat16* H,
                                 int d, __nv_bfloat16* Ht, int* flags, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  k_vshard_lse<<<(rows + 255) / 256, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
-                                                  guard, lse);
-  cudaError_t e = cudaGetLastError();
+  const cudaError_t e = launch_k(k_vshard_lse, (rows + 255) / 256, 256, 0, s, stats, R, rows, y, y_offset, V_shard,
+                                 V_total, ignore_index, ref, guard, lse);
   if (e != cudaSuccess) return e;
-  k_vshard_scale<<<(rows + 7) / 8, 256, 0, s>>>(stats, R, rows, y, y_offset, V_shard, V_total, ignore_index, ref,
-                                                guard, lse, alpha, P, ldp, reinterpret_cast<const uint4*>(H), d / 8,
-                                                reinterpret_cast<uint4*>(Ht), flags);
-  return cudaGetLastError();
+  return launch_k(k_vshard_scale, (rows + 7) / 8, 256, 0, s, stats, R, rows, y, y_offset, V_shard, V_total,
+                  ignore_index, ref, guard, lse, alpha, P, ldp, reinterpret_cast<const uint4*>(H), d / 8,
+                  reinterpret_cast<uint4*>(Ht), flags);
 }
 
 cudaError_t launch_scale(void* bf16, long long n_bf16, float* f32, long long n_f32, const float* g, int num_sms,
                          cudaStream_t s) {
   if (n_bf16 <= 0 && n_f32 <= 0) return cudaSuccess;
-  k_scale<<<num_sms * 4, 256, 0, s>>>(static_cast<uint4*>(bf16), n_bf16 / 8, reinterpret_cast<float4*>(f32),
-                                      n_f32 / 4, g);
-  return cudaGetLastError();
+  return launch_k(k_scale, num_sms * 4, 256, 0, s, static_cast<uint4*>(bf16), n_bf16 / 8,
+                  reinterpret_cast<float4*>(f32), n_f32 / 4, g);
 }
 
 cudaError_t launch_finalize(const float* loss_i, long long N, const DevStatus* st, float* loss, cudaStream_t s) {
-  k_finalize<<<1, 1024, 0, s>>>(loss_i, N, st, loss);
-  return cudaGetLastError();
+  return launch_k(k_finalize, 1, 1024, 0, s, loss_i, N, st, loss);
 }
 
 }  // namespace lce

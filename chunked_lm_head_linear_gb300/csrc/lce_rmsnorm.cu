@@ -76,6 +76,8 @@ __device__ __forceinline__ void load_row(const uint4* __restrict__ xr, int group
 __global__ void __launch_bounds__(kNormThreads, 2) k_rmsnorm_fwd(const uint4* __restrict__ x, const float* __restrict__ w,
                                                                  long long N, int d, float eps, uint4* __restrict__ H,
                                                                  float* __restrict__ rstd) {
+  grid_dep_wait();
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const long long U = static_cast<long long>(gridDim.x) * (kNormThreads / 32);
   long long i = static_cast<long long>(blockIdx.x) * (kNormThreads / 32) + (threadIdx.x >> 5);
@@ -134,6 +136,8 @@ __global__ void __launch_bounds__(kNormThreads, 3) k_rmsnorm_bwd(const uint4* __
                                                               const float* __restrict__ rstd,
                                                               const uint4* __restrict__ dH, long long N, int d,
                                                               uint4* __restrict__ dx, float* __restrict__ part) {
+  grid_dep_wait();
+  grid_dep_launch();
   extern __shared__ float dw_acc[];  // [d]
   __shared__ float red[kNormThreads / 32][kBwdRowGroup];
   __shared__ float cs_row[kBwdRowGroup];
@@ -237,6 +241,8 @@ __global__ void __launch_bounds__(kNormThreads, 3) k_rmsnorm_bwd(const uint4* __
 // in order, then the warp sums are added in warp order.
 __global__ void __launch_bounds__(32 * kColsumWarps) k_colsum(const float* __restrict__ part, int nblocks, int d,
                                                               float* __restrict__ dw) {
+  grid_dep_wait();
+  grid_dep_launch();
   __shared__ float red[kColsumWarps][33];
   const int lane = threadIdx.x & 31, s = threadIdx.x >> 5;
   const int k = blockIdx.x * 32 + lane;
@@ -265,9 +271,8 @@ cudaError_t launch_rmsnorm_fwd(const void* x, const float* w, long long N, int d
   if (e != cudaSuccess) return e;
   const long long need = (N + kNormThreads / 32 - 1) / (kNormThreads / 32);
   const long long blocks = need < static_cast<long long>(kFwdBlocksPerSm) * sms ? need : kFwdBlocksPerSm * sms;
-  k_rmsnorm_fwd<<<static_cast<unsigned>(blocks), kNormThreads, 0, s>>>(static_cast<const uint4*>(x), w, N, d, eps,
-                                                                       static_cast<uint4*>(H), rstd);
-  return cudaGetLastError();
+  return launch_k(k_rmsnorm_fwd, static_cast<unsigned>(blocks), kNormThreads, 0, s, static_cast<const uint4*>(x), w,
+                  N, d, eps, static_cast<uint4*>(H), rstd);
 }
 
 cudaError_t launch_rmsnorm_bwd(const void* x, const float* w, const float* rstd, const void* dH, long long N, int d,
@@ -280,14 +285,11 @@ cudaError_t launch_rmsnorm_bwd(const void* x, const float* w, const float* rstd,
                                            static_cast<int>(smem));
       if (e != cudaSuccess) return e;
     }
-    k_rmsnorm_bwd<<<nb, kNormThreads, smem, s>>>(static_cast<const uint4*>(x), w, rstd,
-                                                  static_cast<const uint4*>(dH), N, d, static_cast<uint4*>(dx),
-                                                  part);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = launch_k(k_rmsnorm_bwd, nb, kNormThreads, smem, s, static_cast<const uint4*>(x), w, rstd,
+                                   static_cast<const uint4*>(dH), N, d, static_cast<uint4*>(dx), part);
     if (e != cudaSuccess) return e;
   }
-  k_colsum<<<(d + 31) / 32, 32 * kColsumWarps, 0, s>>>(part, N > 0 ? nb : 0, d, dw);
-  return cudaGetLastError();
+  return launch_k(k_colsum, (d + 31) / 32, 32 * kColsumWarps, 0, s, part, N > 0 ? nb : 0, d, dw);
 }
 
 }  // namespace lce
