@@ -190,6 +190,7 @@ RAGGED = [
     (200, 512, 257, 0),      # vocabulary one past a tile
     (37, 16, 1, 0),          # a single class: loss 0, zero gradients
     (600, 16384, 5000, 256), # wide hidden size: 256 k-blocks per logits tile, 64 dW column blocks
+    (300, 64, 1000003, 0),   # a million-word vocabulary: dH parts of 3907 k-blocks, 3-column tail
 ]
 
 
