@@ -704,7 +704,7 @@ def main():
     kernels = {k: {"launches": v["launches"], "ms": round(v["ms"], 3),
                    "share": round(v["ms"] / total_ms, 4) if total_ms else 0.0}
                for k, v in prof.items() if v["launches"]}
-    gpu_launches = sum(v["launches"] for k, v in prof.items() if k != "other")
+    gpu_launches = sum(v["launches"] for k, v in prof.items() if k != "memset")  # every library kernel
     hbm_kernels = {}
     for k in lce.HBM_KINDS:
         v = prof.get(k)

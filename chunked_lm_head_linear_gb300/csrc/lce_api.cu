@@ -250,14 +250,14 @@ enum Kind : int {
   K_GEMM_BWD = 4,       // dH and dW GEMMs of a chunk (one launch)
   K_RMSNORM_FWD = 5,
   K_FINALIZE = 6,
-  K_OTHER = 7,          // memsets, the guard-conditional FWD_GRAD (work counted as 0), gradient scaling
+  K_OTHER = 7,          // the guard-conditional passes (work counted as 0), gradient scaling
   K_LOGITS_REF = 8,
-  K_UNUSED = 9,         // (formerly the separate Ht = alpha H pass, now inside combine)
+  K_MEMSET = 9,         // zeroing dW when there are no tokens (a copy-engine memset, not a kernel)
   K_RMSNORM_BWD = 10,   // norm backward and the column sum of its dw partials
 };
 const char* const kKindNames[LCE_KERNEL_KINDS] = {"prepare",    "logits_stats", "combine",  "logits_grad",
                                                   "gemm_dH_dW", "rmsnorm_fwd",  "finalize", "other",
-                                                  "logits_ref", "unused",       "rmsnorm_bwd"};
+                                                  "logits_ref", "memset",       "rmsnorm_bwd"};
 
 struct ProfRecord {
   int kind;
@@ -647,7 +647,7 @@ int lce_backward(const void* H, const void* W, const int64_t* y, int64_t N, int6
   LCE_TRY(device_check(&c.dev));
   LCE_TRY(prepare(c, grad_loss));
   if (N == 0 && !c.o.accumulate_dW)
-    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
+    LCE_TRY(timed(c.s, K_MEMSET, 4.0 * static_cast<double>(V * d),
                   [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
   for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {
     const int64_t rows = (N - c0) < c.L.C ? (N - c0) : c.L.C;
@@ -676,7 +676,7 @@ int fwd_bwd(const void* H, const void* W, const int64_t* y, int64_t N, int64_t d
   float* loss_i = reinterpret_cast<float*>(c.ws + c.L.loss_i);
   LCE_TRY(prepare(c, grad_loss));
   if (N == 0 && !c.o.accumulate_dW)
-    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V * d),
+    LCE_TRY(timed(c.s, K_MEMSET, 4.0 * static_cast<double>(V * d),
                   [&] { return cuda_rc(cudaMemsetAsync(dW, 0, sizeof(float) * static_cast<size_t>(V * d), c.s)); }));
   if (N == 0) LCE_TRY(record_slice_events(c, sl, 0));
   if (N > 0) LCE_TRY(row_references(c));
@@ -804,7 +804,7 @@ int lce_vshard_backward(const void* H, const void* W_shard, const int64_t* y, in
   LCE_TRY(device_check(&c.dev));
   LCE_TRY(prepare(c, grad_loss));
   if (N == 0 && !c.o.accumulate_dW)
-    LCE_TRY(timed(c.s, K_OTHER, 4.0 * static_cast<double>(V_shard * d), [&] {
+    LCE_TRY(timed(c.s, K_MEMSET, 4.0 * static_cast<double>(V_shard * d), [&] {
       return cuda_rc(cudaMemsetAsync(dW_shard, 0, sizeof(float) * static_cast<size_t>(V_shard * d), c.s));
     }));
   for (int64_t c0 = 0; c0 < N; c0 += c.L.C) {

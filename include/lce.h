@@ -316,7 +316,8 @@ int lce_version(void);
  * step. lce_profile_end() synchronises those events and returns, per kernel
  * kind, the number of launches, their summed device time and their summed
  * algorithmic work (bytes for memory-bound kinds, flops for the GEMMs).
- * Events come from a pool the library owns (created on first use, no device
+ * Every kind is a library kernel except "memset" (dW zeroed by a
+ * cudaMemsetAsync when a call has no tokens). Events come from a pool the library owns (created on first use, no device
  * memory is allocated). Not thread-safe: one profiling thread at a time.
  */
 #define LCE_KERNEL_KINDS 11

@@ -172,6 +172,7 @@ def test_profiler_kind_names(lib):
     assert len(set(names)) == lce.LCE_KERNEL_KINDS
     assert set(lce.GEMM_KINDS) <= set(names)
     assert lib.lce_kernel_name(lce.LCE_KERNEL_KINDS) is None
+    assert "memset" in names   # the one kind that is not a library kernel (bench.py leaves it out of gpu_launches)
 
 
 def test_sliced_bounds_checked_on_host(lib):
