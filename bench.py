@@ -530,21 +530,26 @@ def main():
     # kernels with programmatic stream serialization, so a kernel's launch overlaps the end of
     # the one before it; an event recorded between two kernels makes the second wait for the
     # whole of the first and takes that overlap away. This region is what the plain call does.
+    # An event at each step boundary (not between kernels) also gives the median and the fastest step.
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
     barrier()
-    ev0.record(stream)
-    for _ in range(args.steps):
+    step_ev[0].record(stream)
+    for k in range(args.steps):
         step(H, y)
-    ev1.record(stream)
+        step_ev[k + 1].record(stream)
     barrier()
-    ms_plain = ev0.elapsed_time(ev1)
+    ms_plain = step_ev[0].elapsed_time(step_ev[-1])
+    per_step = sorted(step_ev[k].elapsed_time(step_ev[k + 1]) for k in range(args.steps))
     if world > 1:
         t = torch.tensor([ms_plain], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms_plain = float(t.item())
     no_events = {"value": N * world * args.steps / (ms_plain * 1e-3), "unit": UNIT,
                  "ms_per_step": ms_plain / args.steps,
+                 "ms_per_step_median": per_step[len(per_step) // 2], "ms_per_step_min": per_step[0],
                  "how": "the timed loop again, device-resident inputs, without the event pair around each "
-                        "kernel launch (those events serialise the kernels' programmatic launch overlap)"}
+                        "kernel launch (those events serialise the kernels' programmatic launch overlap); "
+                        "one event per step boundary gives the median and minimum step (this rank)"}
 
     # ---- end to end through the same public call, host buffers: every step's H and y are copied
     # from pinned host memory and every step's loss is read back into pinned host memory. The
