@@ -577,6 +577,37 @@ def test_two_streams_at_once(cuda_lib):
                 assert torch.equal(a, b)
 
 
+def test_stream_order_with_other_kernels_between_calls(cuda_lib):
+    """The library launches its kernels so that each may start while the kernel
+    before it in the stream finishes, and each waits at its start for that
+    kernel to complete. Interleaved with PyTorch kernels on the same stream that
+    rewrite the inputs and read and clear the outputs in between, every call
+    still sees the inputs as the stream left them and leaves outputs the next
+    kernel sees whole: each result equals the same call made alone."""
+    torch = _torch()
+    H, W, y = to_dev(small_inputs(700, 256, 4096, seed=95))
+    Hn = -H
+    ref_pos = cuda_lib.lce_fwd_bwd(H, W, y, chunk_tokens=256)
+    ref_neg = cuda_lib.lce_fwd_bwd(Hn, W, y, chunk_tokens=256)
+    torch.cuda.synchronize()
+    ref_pos = [t.clone() for t in ref_pos]
+    ref_neg = [t.clone() for t in ref_neg]
+    Hx = H.clone()
+    dW = torch.zeros_like(ref_pos[3])
+    outs, dWs = [], []
+    for k in range(4):                     # no host synchronisation inside the loop
+        Hx.neg_()                          # a PyTorch kernel rewrites the input just before the call
+        loss, lse, dH, _ = cuda_lib.lce_fwd_bwd(Hx, W, y, dW=dW, chunk_tokens=256)
+        dWs.append(dW.clone())             # read the output at once
+        dW.zero_()                         # and clear it right after
+        outs.append((loss, lse, dH))
+    torch.cuda.synchronize()
+    for k, ((loss, lse, dH), dWk) in enumerate(zip(outs, dWs)):
+        ref = ref_neg if k % 2 == 0 else ref_pos
+        assert torch.equal(loss, ref[0]) and torch.equal(lse, ref[1]) and torch.equal(dH, ref[2]), k
+        assert torch.equal(dWk, ref[3]), k
+
+
 def test_chunk_size_invariance_and_determinism(cuda_lib):
     """loss, lse and dH are row-local with a fixed vocabulary order: bitwise
     equal for every chunk size; dW differs only by fp32 reassociation."""
